@@ -1,0 +1,376 @@
+"""Pins of the CPU oracle to things other than itself.
+
+Each test checks one oracle function against a closed form, a textbook value,
+brute force on a tiny input, an exact identity of the method, or a special
+case; together they are chosen so that a dropped term, a wrong sign or index,
+or a transposed operand in the oracle fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import wan_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+# ---------------------------------------------------------------- activations
+
+def test_gelu_textbook_values():
+    # GELU(x) = x * Phi(x); Phi(1) = 0.8413447460685429 (standard normal table).
+    # The tanh approximation gives 0.8411919906082768 at 1 and would fail.
+    g = O.gelu(np.array([1.0, -1.0, 0.0, 2.0]))
+    assert g[0] == pytest.approx(0.8413447460685429, abs=1e-15)
+    assert g[1] == pytest.approx(-0.15865525393145707, abs=1e-15)
+    assert g[2] == 0.0
+    assert g[3] == pytest.approx(2 * 0.9772498680518208, abs=1e-14)
+
+
+def test_silu_textbook_values():
+    s = O.silu(np.array([0.0, 1.0, -1.0]))
+    assert s[0] == 0.0
+    assert s[1] == pytest.approx(1.0 / (1.0 + math.e ** -1), abs=1e-15)
+    assert s[2] == pytest.approx(-1.0 / (1.0 + math.e), abs=1e-15)
+
+
+# ---------------------------------------------------------------- LayerNorm / modulation
+
+def test_layer_norm_moments_and_affine_invariance():
+    x = rng.normal(size=(7, 64)) * 3 + 1.5
+    y = O.layer_norm(x, 1e-6)
+    assert np.allclose(y.mean(-1), 0.0, atol=1e-14)
+    var = x.var(-1)
+    assert np.allclose(y.var(-1), var / (var + 1e-6), atol=1e-13)
+    # invariant to x -> a x + c per row (a > 0), up to the eps term
+    y2 = O.layer_norm(4.0 * x - 7.0, 1e-12)
+    assert np.allclose(y2, O.layer_norm(x, 1e-12), atol=1e-12)
+
+
+def test_layer_norm_constant_row_is_zero():
+    assert np.all(O.layer_norm(np.full((2, 8), 3.25), 1e-6) == 0.0)
+
+
+def test_modulate_zero_is_identity():
+    y = rng.normal(size=(5, 16))
+    assert np.array_equal(O.modulate(y, 0.0, 0.0), y)
+    assert np.allclose(O.modulate(y, 1.0, -1.0), 1.0)
+
+
+# ---------------------------------------------------------------- time embedding
+
+def test_sinusoid_closed_forms():
+    # tau = 0: all cosines 1, all sines 0
+    s0 = O.sinusoid(np.array([0.0]))[0]
+    assert np.array_equal(s0[:128], np.ones(128)) and np.array_equal(s0[128:], np.zeros(128))
+    # w_0 = 1: tau = pi/2 gives cos = 0 and sin = 1 in the first pair
+    s = O.sinusoid(np.array([math.pi / 2 / 1000]))[0]
+    assert abs(s[0]) < 1e-15 and s[128] == pytest.approx(1.0, abs=1e-15)
+    # w_64 = 10000^(-1/2) = 1/100: tau = 100 pi gives cos(pi) = -1, sin(pi) = 0
+    s = O.sinusoid(np.array([100 * math.pi / 1000]))[0]
+    assert s[64] == pytest.approx(-1.0, abs=1e-12) and abs(s[128 + 64]) < 1e-12
+    assert np.allclose(s[:128] ** 2 + s[128:] ** 2, 1.0, atol=1e-15)
+
+
+def test_time_embedding_zero_weights():
+    D = 8
+    w = {"t1_w": np.zeros((D, 256)), "t1_b": np.full(D, 0.5), "t2_w": np.zeros((D, D)),
+         "t2_b": np.full(D, 1.0), "m_w": np.zeros((6 * D, D)), "m_b": np.arange(6 * D) * 0.1,
+         "hm_w": np.ones((2 * D, D)), "hm_b": np.zeros(2 * D)}
+    e, e0, hm = O.time_embedding(np.array([0.3, 0.9]), w, D)
+    assert np.array_equal(e, np.ones((2, D)))              # e = b2
+    assert np.allclose(e0[1, 2], np.arange(2 * D, 3 * D) * 0.1)   # gate1 slot = third D-chunk of bm
+    silu1 = 1.0 / (1.0 + math.exp(-1.0))
+    assert np.allclose(hm, D * silu1)                       # ones-matrix times SiLU(1)
+
+
+# ---------------------------------------------------------------- RoPE
+
+def test_rope_axis_split():
+    assert O.rope_axis_dims(128) == (44, 42, 42)
+    assert O.rope_axis_dims(64) == (24, 20, 20)
+
+
+def test_rope_preserves_pair_norms_and_zero_position_is_identity():
+    grid = (3, 4, 5)
+    x = rng.normal(size=(60, 2, 64))
+    pos = O.token_positions(grid)
+    y = O.rope3d(x, pos)
+    assert np.allclose(x[..., 0::2] ** 2 + x[..., 1::2] ** 2, y[..., 0::2] ** 2 + y[..., 1::2] ** 2, atol=1e-13)
+    assert np.array_equal(y[0], x[0])          # token 0 sits at (0,0,0)
+
+
+def test_rope_dot_product_depends_only_on_relative_offset():
+    d = 64
+    q = rng.normal(size=(1, 1, d))
+    k = rng.normal(size=(1, 1, d))
+    pa, pb = np.array([[2, 1, 3]]), np.array([[0, 4, 1]])
+    ref = np.sum(O.rope3d(q, pa) * O.rope3d(k, pb))
+    for shift in ([1, 0, 0], [0, 2, 0], [0, 0, 5], [3, 1, 2]):
+        s = np.array([shift])
+        assert np.sum(O.rope3d(q, pa + s) * O.rope3d(k, pb + s)) == pytest.approx(ref, abs=1e-12)
+    # a different relative offset gives a different score
+    assert abs(np.sum(O.rope3d(q, pa) * O.rope3d(k, pb + np.array([[1, 0, 0]]))) - ref) > 1e-6
+
+
+def test_rope_axis_layout_frame_height_width():
+    # Only the first d_f dims rotate with the frame index, the next d_h with the
+    # height index, the last d_w with the width index.
+    d = 128
+    df, dh, dw = O.rope_axis_dims(d)
+    x = rng.normal(size=(1, 1, d))
+    yf = O.rope3d(x, np.array([[1, 0, 0]]))
+    yh = O.rope3d(x, np.array([[0, 1, 0]]))
+    yw = O.rope3d(x, np.array([[0, 0, 1]]))
+    ch = lambda y: np.flatnonzero(np.abs(y - x)[0, 0] > 0)
+    assert ch(yf).min() == 0 and ch(yf).max() < df
+    assert ch(yh).min() >= df and ch(yh).max() < df + dh
+    assert ch(yw).min() >= df + dh and ch(yw).max() < d
+
+
+def test_rope_reduces_to_textbook_1d_rope():
+    # With the token grid (L, 1, 1) only the frame axis moves.  On the frame part
+    # this must equal RoFormer's rotary embedding: pair j of position p is the
+    # complex number (x_2j + i x_2j+1) multiplied by exp(i p theta^(-2j/d_f)).
+    d, L, theta = 64, 7, 10000.0
+    df = O.rope_axis_dims(d)[0]
+    x = rng.normal(size=(L, 1, d))
+    y = O.rope3d(x, O.token_positions((L, 1, 1)), theta)
+    for p in range(L):
+        for j in range(df // 2):
+            z = complex(x[p, 0, 2 * j], x[p, 0, 2 * j + 1]) * np.exp(1j * p * theta ** (-2 * j / df))
+            assert y[p, 0, 2 * j] == pytest.approx(z.real, abs=1e-12)
+            assert y[p, 0, 2 * j + 1] == pytest.approx(z.imag, abs=1e-12)
+    assert np.array_equal(y[..., df:], x[..., df:])
+
+
+def test_token_positions_order():
+    pos = O.token_positions((2, 3, 4))
+    assert pos[0].tolist() == [0, 0, 0]
+    assert pos[1].tolist() == [0, 0, 1]       # width fastest
+    assert pos[4].tolist() == [0, 1, 0]
+    assert pos[12].tolist() == [1, 0, 0]
+    assert pos[23].tolist() == [1, 2, 3]
+
+
+# ---------------------------------------------------------------- attention
+
+def _brute_attention(q, k, v):
+    Lq, H, d = q.shape
+    Lk = k.shape[0]
+    out = np.zeros((Lq, H, v.shape[-1]))
+    for h in range(H):
+        for i in range(Lq):
+            logits = [sum(q[i, h, c] * k[j, h, c] for c in range(d)) / math.sqrt(d) for j in range(Lk)]
+            m = max(logits)
+            ws = [math.exp(a - m) for a in logits]
+            z = sum(ws)
+            for c in range(v.shape[-1]):
+                out[i, h, c] = sum(ws[j] * v[j, h, c] for j in range(Lk)) / z
+    return out
+
+
+def test_attention_brute_force():
+    q = rng.normal(size=(5, 2, 4)) * 2
+    k = rng.normal(size=(7, 2, 4)) * 2
+    v = rng.normal(size=(7, 2, 4))
+    assert np.allclose(O.attention(q, k, v), _brute_attention(q, k, v), atol=1e-13)
+    # row chunking must not change anything
+    assert np.allclose(O.attention(q, k, v, chunk=2), O.attention(q, k, v), atol=1e-15)
+
+
+def test_attention_special_cases():
+    q = rng.normal(size=(6, 3, 8))
+    v1 = rng.normal(size=(1, 3, 8))
+    assert np.allclose(O.attention(q, rng.normal(size=(1, 3, 8)), v1), np.broadcast_to(v1, (6, 3, 8)), atol=1e-15)
+    kc = np.broadcast_to(rng.normal(size=(1, 3, 8)), (9, 3, 8))
+    v = rng.normal(size=(9, 3, 8))
+    assert np.allclose(O.attention(q, kc, v), np.broadcast_to(v.mean(0), (6, 3, 8)), atol=1e-14)
+    # large logits select the best-matching key
+    k = np.eye(8)[:, None, :].repeat(3, axis=1) * 1e3
+    qq = np.eye(8)[[2, 5], None, :].repeat(3, axis=1)
+    v = rng.normal(size=(8, 3, 8))
+    o = O.attention(qq, k, v)
+    assert np.allclose(o[0], v[2], atol=1e-12) and np.allclose(o[1], v[5], atol=1e-12)
+    # outputs are convex combinations of the values
+    o = O.attention(q, rng.normal(size=(9, 3, 8)), v[:1].repeat(9, 0) + rng.normal(size=(9, 3, 8)))
+    assert o.shape == (6, 3, 8)
+
+
+def test_attention_convexity():
+    q, k, v = rng.normal(size=(4, 1, 8)) * 3, rng.normal(size=(10, 1, 8)) * 3, rng.normal(size=(10, 1, 8))
+    o = O.attention(q, k, v)
+    assert np.all(o <= v.max(0) + 1e-12) and np.all(o >= v.min(0) - 1e-12)
+
+
+# ---------------------------------------------------------------- patchify / unpatchify
+
+def test_patchify_index_formula_brute_force():
+    B, C, F, H, W = 2, 3, 2, 4, 6
+    lat = rng.normal(size=(B, C, F, H, W))
+    p = O.patchify_tokens(lat)
+    Hp, Wp = H // 2, W // 2
+    for b in range(B):
+        for c in range(C):
+            for f in range(F):
+                for y in range(H):
+                    for x in range(W):
+                        i, di, j, dj = y // 2, y % 2, x // 2, x % 2
+                        assert p[b, (f * Hp + i) * Wp + j, c * 4 + di * 2 + dj] == lat[b, c, f, y, x]
+
+
+def test_patchify_identity_weight_and_unpatchify_roundtrip():
+    B, C, F, H, W = 1, 4, 3, 6, 4
+    lat = rng.normal(size=(B, C, F, H, W))
+    x = O.patchify(lat, np.eye(C * 4), np.zeros(C * 4))
+    assert np.array_equal(x, O.patchify_tokens(lat))
+    assert np.array_equal(O.unpatchify(x, C, F, H, W), lat)
+
+
+def test_patchify_i2v_zero_columns():
+    # I2V: extra input channels with zero-initialised projection columns leave the
+    # 16-channel result unchanged.
+    D = 8
+    lat16 = rng.normal(size=(1, 16, 2, 4, 4))
+    extra = rng.normal(size=(1, 20, 2, 4, 4))
+    w16 = rng.normal(size=(D, 64))
+    b = rng.normal(size=D)
+    w36 = np.concatenate([w16, np.zeros((D, 80))], axis=1)
+    a = O.patchify(lat16, w16, b)
+    c = O.patchify(np.concatenate([lat16, extra], axis=1), w36, b)
+    assert np.allclose(a, c, atol=1e-14)
+
+
+# ---------------------------------------------------------------- guidance and Euler
+
+def test_cfg_special_cases():
+    vc, vu = rng.normal(size=(3, 5)), rng.normal(size=(3, 5))
+    assert np.allclose(O.cfg_combine(vc, vu, 1.0), vc, rtol=0, atol=1e-15)
+    assert np.array_equal(O.cfg_combine(vc, vu, 0.0), vu)
+    a, b = O.cfg_combine(vc, vu, 2.0), O.cfg_combine(vc, vu, 5.0)
+    assert np.allclose(O.cfg_combine(vc, vu, 3.5), (a + b) / 2, atol=1e-14)   # affine in s
+
+
+def test_euler_exact_velocity_lands_on_data():
+    # x_t = t x0 + (1 - t) x1 (t = 1 noise, t = 0 data); dx/dt = x0 - x1.
+    x0, x1 = rng.normal(size=100), rng.normal(size=100)
+    v = x0 - x1
+    assert np.allclose(O.euler_step(x0, v, -1.0), x1, atol=1e-15)
+    x = x0.copy()
+    ts = O.timesteps(20)
+    assert ts[0] == 1.0 and ts[-1] == 0.0 and len(ts) == 21
+    for k in range(20):
+        x = O.euler_step(x, v, ts[k + 1] - ts[k])
+    assert np.allclose(x, x1, atol=1e-14)
+
+
+def test_euler_zero_velocity_and_cfg_euler():
+    x = rng.normal(size=10)
+    assert np.array_equal(O.euler_step(x, np.zeros(10), -0.05), x)
+    vc, vu = rng.normal(size=10), rng.normal(size=10)
+    assert np.allclose(O.cfg_euler_step(x, vc, vu, 1.0, -0.05), x - 0.05 * vc, atol=1e-15)
+
+
+# ---------------------------------------------------------------- block / forward
+
+def _tiny(seed=0, **kw):
+    s = synth.CONFIGS[0].replace(**kw)
+    w = synth.make_weights(s, seed)
+    inp = synth.make_inputs(s, seed)
+    return s, w, inp
+
+
+def _ctx(s, w, inp):
+    return O.text_projection(inp["text"], w)
+
+
+def test_adaln_zero_reduces_block_to_residual_path():
+    s, w, inp = _tiny()
+    hp = O.Hyper.of(s)
+    blk = dict(w["blocks"][0])
+    x = rng.normal(size=(s.tokens, s.dim))
+    ctx = _ctx(s, w, inp)[0]
+    zero = np.zeros((6, s.dim))
+    out = O.dit_block(x, zero, blk, ctx, None, hp)
+    expect = x + O.cross_attention(x, blk, ctx, None, hp)
+    assert np.allclose(out, expect, atol=1e-14)
+    blk["co_w"] = np.zeros_like(blk["co_w"])
+    blk["co_b"] = np.zeros_like(blk["co_b"])
+    assert np.array_equal(O.dit_block(x, zero, blk, ctx, None, hp), x)
+
+
+def test_block_row_sampling_matches_full_block():
+    s, w, inp = _tiny()
+    hp = O.Hyper.of(s)
+    blk = w["blocks"][0]
+    x = rng.normal(size=(s.tokens, s.dim))
+    ctx = _ctx(s, w, inp)[0]
+    mods = rng.normal(size=(6, s.dim)) * 0.1
+    full = O.dit_block(x, mods, blk, ctx, None, hp)
+    rows = np.array([0, 5, 17, s.tokens - 1])
+    assert np.allclose(O.dit_block(x, mods, blk, ctx, None, hp, rows=rows), full[rows], atol=1e-13)
+
+
+def test_decoupled_cross_attention_sums_two_softmaxes():
+    s, w, inp = _tiny(img_len=5, i2v=False)
+    hp = O.Hyper.of(s)
+    blk = dict(w["blocks"][0])
+    blk["ckvi_w"], blk["ckvi_b"] = blk["ckv_w"], blk["ckv_b"]
+    x = rng.normal(size=(10, s.dim))
+    ctx = _ctx(s, w, inp)[0]
+    one = O.cross_attention(x, blk, ctx, None, hp) - blk["co_b"]
+    two = O.cross_attention(x, blk, ctx, ctx, hp) - blk["co_b"]
+    assert np.allclose(two, 2 * one, atol=1e-13)
+
+
+def test_forward_batch_permutation_equivariance():
+    s, w, inp = _tiny()
+    ctx = _ctx(s, w, inp)
+    lat = np.concatenate([inp["latent"], 0.5 * inp["latent"]], axis=0)
+    t = np.array([0.3, 0.8])
+    v = O.dit_forward(lat, t, ctx, None, w, s)
+    vp = O.dit_forward(lat[::-1], t[::-1], ctx[::-1], None, w, s)
+    assert np.allclose(v[::-1], vp, atol=1e-13)
+    assert v.shape == (2, s.c_out, s.frames, s.height, s.width)
+
+
+def test_forward_row_sampling_matches_full_forward():
+    s, w, inp = _tiny()
+    ctx = _ctx(s, w, inp)
+    lat = np.concatenate([inp["latent"]] * 2, axis=0)
+    t = np.array([0.4, 0.4])
+    v = O.dit_forward(lat, t, ctx, None, w, s)
+    rows = np.array([1, 9, 47])
+    hv, _ = O.dit_forward(lat, t, ctx, None, w, s, rows=rows)
+    tok = O.patchify_tokens(v)          # head outputs arranged as tokens
+    assert np.allclose(hv, tok[:, rows], atol=1e-13)
+
+
+def test_guided_step_with_scale_one_is_conditional_euler():
+    s, w, inp = _tiny(guide_scale=1.0)
+    ctx = _ctx(s, w, inp)
+    t = float(inp["t"][0])
+    xn = O.guided_step(inp["latent"], t, -0.05, ctx, None, w, s)
+    v = O.dit_forward(inp["latent"], np.array([t]), ctx[:1], None, w, s)
+    assert np.allclose(xn, inp["latent"] - 0.05 * v, atol=1e-14)
+
+
+# ---------------------------------------------------------------- geometry fixture
+
+def test_latent_geometry_fixture():
+    with open(os.path.join(GOLDEN, "latent_geometry.json")) as f:
+        g = json.load(f)
+    for case in g["cases"]:
+        T1, H, W = case["video"]
+        lat = [1 + (T1 - 1) // g["compression"][0], H // g["compression"][1], W // g["compression"][2]]
+        assert lat == case["latent"]
+        tokens = lat[0] * (lat[1] // 2) * (lat[2] // 2)
+        assert tokens == case["tokens"]
+        cfg = synth.CONFIGS[case["config"]]
+        assert [cfg.frames, cfg.height, cfg.width] == lat and cfg.tokens == tokens
+    c, s_ = g["i2v_channels"]["c"], g["i2v_channels"]["s"]
+    assert 2 * c + s_ == synth.CONFIGS[3].c_in
