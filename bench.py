@@ -1,0 +1,364 @@
+#!/usr/bin/env python
+"""Benchmark of the Wan DiT guided denoising step on B300 (libwan, sm_103a).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 2]
+
+One step = one pass of the whole hot path over the 30-block 1.3B-shaped DiT at 480p
+(21x60x104 latent -> 32760 tokens), batch 2 (cond + uncond): text projection, time
+embedding, patchify, 30 blocks (AdaLN, QKV + 3D RoPE, self-attention, cross-attention,
+GELU FFN, gated residuals), head + depatchify, fused CFG + Euler update.  Synthetic
+seeded inputs, random-init weights ~N(0, 0.02).  Rank 0 prints one JSON line.
+
+--impl reference times the CPU fp64 oracle (the method's plain definition) on the
+host cores, on a bounded sample of the same workload, and extrapolates to one step.
+Multi-GPU: the step does not shard (self-attention couples every token); N ranks run
+N independent replicas (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "DiT step latent tokens/s and bf16 TFLOP/s on 1 B300; % of BF16 tensor peak"
+UNIT = "latent tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def step_macs(s) -> dict:
+    """Algorithmic multiply-accumulates of one guided step, by role."""
+    B, L, D, F, Lt, Li = s.batch, s.tokens, s.dim, s.ffn, s.text_len, s.img_len
+    m = {
+        "text": B * Lt * (s.text_dim * D + D * D) if s.text_dim else 0,
+        "time": B * (s.freq_dim * D + D * D + 6 * D * D + 2 * D * D),
+        "patchify": B * L * s.c_in * 4 * D,
+        "qkv": s.blocks * B * L * 3 * D * D,
+        "self_attn": s.blocks * B * 2 * L * L * D,
+        "o": s.blocks * B * L * D * D,
+        "cross_q_o": s.blocks * B * L * 2 * D * D,
+        "cross_kv": s.blocks * B * (Lt + Li) * 2 * D * D,
+        "cross_attn": s.blocks * B * 2 * L * (Lt + Li) * D,
+        "ffn": s.blocks * B * L * 2 * D * F,
+        "head": B * L * D * s.c_out * 4,
+    }
+    return m
+
+
+# ---------------------------------------------------------------- clocks during the timed region
+
+class Clocks:
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown," \
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
+             "clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.file.flush()
+        self.file.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, flag in zip(names, parts[3:7]):
+                if flag.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.file.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+
+def oracle_step_estimate(s, seed=0, rows_small=16, rows_large=48):
+    """Time the fp64 oracle on a bounded sample of one block and extrapolate to a step.
+
+    Sample: one 1.3B-shaped block on batch entry 0 with every key/value row (LN, QKV over
+    all L tokens) and `rows` query rows through attention, cross-attention and the FFN,
+    at two row counts; block time = fixed + L * per_row; step = batch * blocks * block.
+    """
+    from oracle import wan_oracle as O
+    from threadpoolctl import threadpool_info
+    one = s.replace(blocks=1)
+    w = synth.make_weights(one, seed)
+    inp = synth.make_inputs(one, seed)
+    hp = O.Hyper.of(one)
+    blk = w["blocks"][0]
+    x = O.patchify(inp["latent"], w["patch_w"], w["patch_b"])[0]
+    ctx = O.text_projection(inp["text"][:1], w)[0] if one.text_dim else inp["ctx_txt"][0]
+    mods = np.zeros((6, one.dim))
+    times = {}
+    for n in (rows_small, rows_large):
+        rows = np.arange(n)
+        t0 = time.perf_counter()
+        O.dit_block(x, mods, blk, ctx, None, hp, rows=rows)
+        times[n] = time.perf_counter() - t0
+    per_row = max((times[rows_large] - times[rows_small]) / (rows_large - rows_small), 1e-12)
+    fixed = max(times[rows_small] - rows_small * per_row, 0.0)
+    block = fixed + one.tokens * per_row
+    step = block * s.batch * s.blocks
+    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    sample = (f"one {one.dim}-wide block, batch entry 0: full LN+QKV over {one.tokens} tokens plus "
+              f"{rows_small} and {rows_large} query rows end to end ({sum(times.values()):.1f} s of CPU); "
+              f"extrapolated x{s.batch} batch x{s.blocks} blocks")
+    return step, threads, sample, sum(times.values())
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(a, s):
+    import torch
+    import torch.distributed as dist
+
+    from video_diffusion_transformer_04_b300 import wan
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+
+    w = synth.make_weights(s, 0)
+    inp = synth.make_inputs(s, 0)
+    m = wan.DiT(s, w, device=dev)
+    del w
+    bf = torch.bfloat16
+    text_h = torch.from_numpy(inp["text"]).to(bf).pin_memory() if s.text_dim else None
+    lat_h = torch.from_numpy(inp["latent"]).pin_memory()
+    t0 = float(inp["t"][0])
+    t_pair_h = torch.tensor([t0, t0 + s.dt], dtype=torch.float32).pin_memory()
+    text = text_h.to(dev) if s.text_dim else None
+    ctx_fixed = None if s.text_dim else torch.from_numpy(inp["ctx_txt"]).to(dev, bf)
+    ctx_img = torch.from_numpy(inp["ctx_img"]).to(dev, bf) if s.img_len else None
+    x = lat_h.to(dev)
+    t_pair = t_pair_h.to(dev)
+    v_ws = torch.empty(2, s.c_out, s.frames, s.height, s.width, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ctx = m.text_embed(text) if s.text_dim else ctx_fixed
+        m.guided_step(x, t_pair, s.guide_scale, ctx, ctx_img, v_ws=v_ws)
+
+    for _ in range(a.warmup):
+        step()
+    wan.wan_sync_status()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = str(getattr(props, "uuid", local))
+    if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) == 36:
+        gpu_id = "GPU-" + gpu_id
+    clocks = Clocks(gpu_id)
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = wan.wan_launch_count()
+    wan.wan_profile_begin(1 << 17)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(a.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    prof = wan.wan_profile_end()
+    launches = wan.wan_launch_count() - launches0
+    clk = clocks.stop()
+    wan.wan_sync_status()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    # ---- end to end through the public API with host buffers (copies inside the timed region)
+    x_out_h = torch.empty_like(lat_h).pin_memory()
+    h2d = lat_h.numel() * 4 + t_pair_h.numel() * 4 + (text_h.numel() * 2 if s.text_dim else 0)
+    d2h = x_out_h.numel() * 4
+
+    def step_host():
+        x.copy_(lat_h, non_blocking=True)
+        t_pair.copy_(t_pair_h, non_blocking=True)
+        if s.text_dim:
+            text.copy_(text_h, non_blocking=True)
+        step()
+        x_out_h.copy_(x, non_blocking=True)
+
+    step_host()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(a.steps):
+        step_host()
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = f0.elapsed_time(f1)
+    if world > 1:
+        tt = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_e2e = float(tt.item())
+
+    tokens_per_step = s.batch * s.tokens
+    value = tokens_per_step * a.steps * world / (ms / 1e3)
+    macs = step_macs(s)
+    flop_step = 2 * sum(macs.values())
+    pk, pk_kind = peaks()
+    tflops = flop_step * a.steps / (ms / 1e3) / 1e12
+
+    total_prof = sum(v[0] for v in prof.values()) or 1.0
+    kernels = {k: {"ms_per_step": round(v[0] / a.steps, 3), "launches_per_step": v[1] / a.steps,
+                   "share": round(v[0] / total_prof, 4)} for k, v in sorted(prof.items(), key=lambda kv: -kv[1][0])}
+    dom = "attn_self"
+    roof = None
+    if dom in prof:
+        per_launch_flop = 2 * macs["self_attn"] / (s.blocks)   # one launch = one block, whole batch
+        avg_ms = prof[dom][0] / prof[dom][1]
+        achieved = per_launch_flop / (avg_ms / 1e3) / 1e12
+        peak = pk["bf16_tflops_sustained"]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "peak_kind": f"bf16 sustained ({pk_kind})",
+                "flop_per_launch": per_launch_flop, "avg_launch_ms": round(avg_ms, 4),
+                "traffic": traffic_record(dom)}
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": round(ms / a.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) latent and text, N(0,0.02) weights)",
+        "config": {"workload": f"config {a.config}: {s.name}", "blocks": s.blocks, "batch": s.batch,
+                   "latent": [s.c_in, s.frames, s.height, s.width], "tokens": s.tokens, "dim": s.dim,
+                   "heads": s.heads, "head_dim": s.head_dim, "ffn": s.ffn, "text_len": s.text_len,
+                   "img_len": s.img_len, "guide_scale": s.guide_scale,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: 2.8 GB of weights and ~3 GB of activations stream every step"},
+        "tflops": round(tflops, 1), "bf16_peak_frac": round(tflops / pk["bf16_tflops"], 4),
+        "bf16_sustained_frac": round(tflops / pk["bf16_tflops_sustained"], 4),
+        "flop_per_step": flop_step,
+        "roofline": roof,
+        "e2e": {"value": round(tokens_per_step * a.steps * world / (ms_e2e / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "kernels": kernels,
+    }
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        step_s, threads, sample, spent = oracle_step_estimate(s)
+        out["cpu_baseline"] = {"value": round(tokens_per_step / step_s, 3), "unit": UNIT, "cores": threads,
+                               "kind": "oracle", "sample": sample, "cpu_seconds": round(spent, 1),
+                               "step_seconds_extrapolated": round(step_s, 1)}
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def traffic_record(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it still matches the source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        import hashlib
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+        if not rec:
+            return None
+        src = os.path.join(ROOT, "video_diffusion_transformer_04_b300", "csrc", rec["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if h != rec["source_sha256_16"]:
+            return None
+        return rec["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- reference arm (CPU oracle)
+
+def run_reference(a, s):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    est = []
+    threads, sample = 1, ""
+    for i in range(a.warmup + a.steps):
+        step_s, threads, sample, _ = oracle_step_estimate(s, rows_small=8, rows_large=24)
+        if i >= a.warmup:
+            est.append(step_s)
+    step_s = statistics.mean(est)
+    value = s.batch * s.tokens / step_s
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1,
+           "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(step_s * 1e3, 1), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": f"config {a.config}: {s.name}", "tokens": s.tokens, "blocks": s.blocks,
+                      "batch": s.batch},
+           "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    s = synth.CONFIGS[a.config]
+    if a.config in (1, 3):
+        s = s.replace(batch=2)  # guided step over a single block: cond + uncond
+    if a.impl == "reference":
+        run_reference(a, s)
+    else:
+        run_ours(a, s)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+/*
+ * wan.h - C ABI of libwan: the Wan video-DiT denoising step on one B300 (sm_103a).
+ *
+ * Sources of the operations (cited by page title and section):
+ *   [Method]  hyper.ai summary of "Wan: Open and Advanced Large-Scale Video Generative
+ *             Models" (arXiv 2503.20314), section "方法" (Method): patchify by a (1,2,2)
+ *             3D conv into (B, L, D); transformer blocks with text cross-attention; an MLP
+ *             of Linear + SiLU on the time embedding predicting six modulation
+ *             parameters; a depatchify module; flow matching on the linear path between
+ *             data x1 and noise x0.
+ *   [Code]    zizhi168.cn "阿里Wan 2.1视频生成模型深度剖析", section "核心代码实现亮点":
+ *             the classifier-free guidance combination, DiT-style modulation, self- and
+ *             cross-attention per block, rope_apply(q|k, grid_sizes, freqs) before
+ *             flash_attention, CLIP context concatenated ahead of the text context.
+ *   [I2V]     x-humanoid.csdn.net notes on the Wan report, section 1.1 "模型设计": noise,
+ *             condition latent and mask concatenated on channels, zero-initialised extra
+ *             projection, decoupled cross-attention to CLIP image features.
+ *   [Sampler] kwkr.cn hands-on article, sections 3.2 and 4.4: Euler integration,
+ *             about 20 steps, latent = latent + v*dt.
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor argument is a DEVICE pointer owned by the caller.  libwan never
+ *     allocates, frees or retains device memory; the only scratch is the caller's
+ *     workspace (ws, ws_bytes), sized by the matching *_workspace_size function.
+ *   - Layouts are dense row-major (C order), 16-byte aligned; the workspace 1024-byte
+ *     aligned.  Token order inside a sample is (f, i, j) with j fastest, i.e. token
+ *     l = (f*Hp + i)*Wp + j on the patch grid (Fg, Hp, Wp) = (F, H/2, W/2).
+ *   - Weights use the nn.Linear layout [out, in].  With dtype WAN_BF16 every weight,
+ *     bias and activation argument is bf16 (fp32 accumulation); with WAN_F32 they are
+ *     fp32 (the parity path).  The residual stream x, the latent and the velocity are
+ *     always fp32.
+ *   - Everything is enqueued asynchronously on `stream` (NULL = legacy default stream).
+ *   - Return value: WAN_OK (0) or a negative status.  Arguments are validated on the
+ *     host before anything is launched; on an error nothing, or only a prefix of the
+ *     work, has been enqueued and the outputs are undefined.  Kernels never trap: a
+ *     pipeline wait that exceeds its time limit sets a device status word that
+ *     wan_sync_status() reports as WAN_ERR_TIMEOUT.  There is no CPU fallback.
+ */
+#ifndef WAN_H_
+#define WAN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* wan_stream_t; /* identical to cudaStream_t */
+
+enum wan_status_code {
+  WAN_OK = 0,
+  WAN_ERR_INVALID_ARG = -1, /* NULL pointer, non-positive size, inconsistent shape */
+  WAN_ERR_UNSUPPORTED = -2, /* shape/alignment/dtype the kernels do not handle */
+  WAN_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed */
+  WAN_ERR_TIMEOUT = -4,     /* a device pipeline wait ran out of time */
+  WAN_ERR_WORKSPACE = -5    /* ws NULL, misaligned or smaller than required */
+};
+
+enum wan_dtype { WAN_BF16 = 0, WAN_F32 = 1 };
+
+/* Epilogues of wan_linear: y = x W^T + b followed by ... */
+enum wan_epilogue {
+  WAN_EPI_STORE = 0,    /* store y in out_dtype */
+  WAN_EPI_GELU = 1,     /* store GELU(y) (erf form) in out_dtype */
+  WAN_EPI_RESIDUAL = 2  /* x_f32[m, n] += gate[m / rows_per_gate, n] * y (gate NULL: 1) */
+};
+
+/* Human-readable text of a status code (static storage). */
+const char* wan_status_string(int status);
+
+/* Synchronise `stream`, then read and clear the device status word of the current
+ * device.  Returns WAN_ERR_TIMEOUT if any kernel since the last call gave up on a
+ * pipeline wait, WAN_ERR_CUDA if the synchronisation failed, else WAN_OK. */
+int wan_sync_status(wan_stream_t stream);
+
+/* Number of libwan kernels launched by this process so far (all devices). */
+long long wan_launch_count(void);
+
+/* ------------------------------------------------------------------ patchify
+ * [Method] patchify: a 3D conv with kernel = stride = (1,2,2) maps the latent
+ * [B, C, F, H, W] to the token sequence x [B, L, D], L = F*(H/2)*(W/2):
+ *   x[b, l, :] = bias + sum_{c,di,dj} w[:, c*4 + di*2 + dj] * latent[b, c, f, 2i+di, 2j+dj].
+ * latent: fp32 [B, C, F, H, W] (H, W even).  w: [D, C*4], b: [D] (dtype).
+ * x: fp32 [B, L, D] (the residual stream; overwritten).
+ * ws: >= wan_patchify_workspace_size(...) bytes (the gathered patches).
+ * Needs D % 32 == 0. */
+size_t wan_patchify_workspace_size(int B, int C, int F, int H, int W, int dtype);
+int wan_patchify(const float* latent, const void* w, const void* b, float* x, int B, int C, int F,
+                 int H, int W, int D, int dtype, void* ws, size_t ws_bytes, wan_stream_t stream);
+
+/* ------------------------------------------------------------------ AdaLN
+ * [Code] DiT-style modulation: y = LN(x) * (1 + scale[b]) + shift[b], LN over D with
+ * biased variance, no affine, epsilon eps.  x: fp32 [B, L, D]; shift, scale: fp32 [B, D]
+ * (both NULL: plain LN).  y: [B, L, D] in dtype.  Needs D % 4 == 0, D <= 8192. */
+int wan_adaln_modulate(const float* x, const float* shift, const float* scale, void* y, int B, int L,
+                       int D, float eps, int dtype, wan_stream_t stream);
+
+/* ------------------------------------------------------------------ self-attention
+ * [Code] x = flash_attention(q=rope_apply(q, grid_sizes, freqs), k=rope_apply(k, ...), v):
+ * full bidirectional softmax(q k^T / sqrt(d)) v per (batch, head), no mask.
+ * 3D RoPE: the head dim splits into [frame | height | width] parts of sizes
+ * (d - 4*floor(d/6), 2*floor(d/6), 2*floor(d/6)); adjacent pairs (2m, 2m+1) of part a
+ * rotate by pos_a * theta^(-2j/d_a), pos = the token's (f, i, j) on the grid
+ * (Fg, Hg, Wg), Fg*Hg*Wg == L.
+ * q, k, v, o: [B, L, H, d] (dtype).  apply_rope = 0 treats q and k as already rotated.
+ * ws: >= wan_attn_workspace_size(...).  d must be 64 or 128 (bf16 path); d <= 128 and
+ * even (fp32 path). */
+size_t wan_attn_workspace_size(int B, int L, int H, int d, int dtype);
+int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B, int L, int H, int d,
+                    int Fg, int Hg, int Wg, float theta, int apply_rope, int dtype, void* ws,
+                    size_t ws_bytes, wan_stream_t stream);
+
+/* ------------------------------------------------------------------ cross-attention
+ * [Method] text conditioning by cross-attention; [I2V] decoupled cross-attention to the
+ * CLIP image context: o = softmax(q kt^T/sqrt(d)) vt + softmax(q ki^T/sqrt(d)) vi
+ * (the second term only when ki != NULL).
+ * q, o: [B, L, H, d]; kt, vt: [B, Lt, H, d]; ki, vi: [B, Li, H, d] or NULL (dtype).
+ * ws: >= wan_cross_attn_workspace_size(...). */
+size_t wan_cross_attn_workspace_size(int B, int Lt, int Li, int H, int d, int dtype);
+int wan_cross_attn(const void* q, const void* kt, const void* vt, const void* ki, const void* vi,
+                   void* o, int B, int L, int Lt, int Li, int H, int d, int dtype, void* ws,
+                   size_t ws_bytes, wan_stream_t stream);
+
+/* ------------------------------------------------------------------ FFN
+ * FFN sub-layer with gated residual: x += gate[b] * (W2 GELU(W1 y + b1) + b2).
+ * y: [B, L, D] modulated input (dtype); w1: [F, D], b1: [F]; w2: [D, F], b2: [D];
+ * gate: fp32 [B, D] (NULL: 1); x_inout: fp32 [B, L, D]; h_ws: [B, L, F] (dtype) scratch.
+ * Needs D % 32 == 0, F % 32 == 0. */
+int wan_ffn(const void* y, const void* w1, const void* b1, const void* w2, const void* b2,
+            const float* gate, float* x_inout, void* h_ws, int B, int L, int D, int F, int dtype,
+            wan_stream_t stream);
+
+/* ------------------------------------------------------------------ linear
+ * One projection y = x W^T + b with an epilogue (enum wan_epilogue); the GEMM under every
+ * projection of the block.  x: [M, K] (dtype); w: [N, K]; b: [N] or NULL (dtype).
+ * WAN_EPI_STORE / WAN_EPI_GELU write out [M, N] in out_dtype (WAN_BF16 only with
+ * dtype WAN_BF16).  WAN_EPI_RESIDUAL accumulates into the fp32 out [M, N] with the
+ * optional fp32 gate [M / rows_per_gate, N].  Needs K % 8 == 0, N % 32 == 0. */
+int wan_linear(const void* x, const void* w, const void* b, void* out, int M, int N, int K,
+               int epilogue, const float* gate, int rows_per_gate, int dtype, int out_dtype,
+               wan_stream_t stream);
+
+/* ------------------------------------------------------------------ text projection
+ * Projection of the text-encoder output (umT5 width Ct) to the DiT width D.
+ * READING (pages silent on its form): ctx = W2 GELU(W1 text + b1) + b2.
+ * text: [B, Lt, Ct]; w1: [D, Ct], b1: [D]; w2: [D, D], b2: [D]; ctx: [B, Lt, D] (dtype). */
+size_t wan_text_embed_workspace_size(int B, int Lt, int D, int dtype);
+int wan_text_embed(const void* text, const void* w1, const void* b1, const void* w2, const void* b2,
+                   void* ctx, int B, int Lt, int Ct, int D, int dtype, void* ws, size_t ws_bytes,
+                   wan_stream_t stream);
+
+/* ------------------------------------------------------------------ CFG + Euler
+ * [Code] noise_pred = uncond + s * (cond - uncond); [Sampler 4.4] x <- x + v * dt, with
+ * t running from 1 (noise) to 0 (data) and dt = t_next - t:
+ *   x[i] <- x[i] + dt * (v_uncond[i] + guide_scale * (v_cond[i] - v_uncond[i])).
+ * x: fp32 [n] in place; v_cond, v_uncond: [n] in v_dtype (WAN_BF16 or WAN_F32).
+ * n == 0 is a no-op. */
+int wan_cfg_euler_step(float* x, const void* v_cond, const void* v_uncond, long long n,
+                       float guide_scale, float dt, int v_dtype, wan_stream_t stream);
+
+/* ------------------------------------------------------------------ whole DiT forward */
+typedef struct wan_dit_config {
+  int dtype;       /* WAN_BF16 or WAN_F32 */
+  int batch;       /* B */
+  int c_in, c_out; /* latent channels in (16; 36 for I2V) and predicted (16) */
+  int frames, height, width; /* latent F, H, W (H, W even) */
+  int dim, heads, head_dim, ffn, blocks;
+  int text_len;    /* Lt */
+  int img_len;     /* Li (0: text-to-video) */
+  int freq_dim;    /* sinusoid width of the time embedding (256) */
+  float theta;     /* RoPE base (10000) */
+  float eps;       /* LayerNorm epsilon (1e-6) */
+} wan_dit_config;
+
+typedef struct wan_block_weights {
+  const void* mod;                  /* [6, D]  learned bias added to the shared e0 */
+  const void *qkv_w, *qkv_b;        /* [3D, D], [3D] */
+  const void *o_w, *o_b;            /* [D, D], [D] */
+  const void *cq_w, *cq_b;          /* [D, D], [D]   cross-attention query */
+  const void *ckv_w, *ckv_b;        /* [2D, D], [2D] text key|value */
+  const void *ckvi_w, *ckvi_b;      /* [2D, D], [2D] image key|value (NULL when img_len == 0) */
+  const void *co_w, *co_b;          /* [D, D], [D]   cross-attention output */
+  const void *f1_w, *f1_b;          /* [F, D], [F] */
+  const void *f2_w, *f2_b;          /* [D, F], [D] */
+} wan_block_weights;
+
+typedef struct wan_dit_weights {
+  const void *patch_w, *patch_b;    /* [D, c_in*4], [D] */
+  const void *t1_w, *t1_b;          /* [D, freq_dim], [D] */
+  const void *t2_w, *t2_b;          /* [D, D], [D] */
+  const void *m_w, *m_b;            /* [6D, D], [6D]  block modulation (shift1,scale1,gate1,shift2,scale2,gate2) */
+  const void *hm_w, *hm_b;          /* [2D, D], [2D]  head modulation (shift, scale) */
+  const void *head_w, *head_b;      /* [c_out*4, D], [c_out*4] */
+  const wan_block_weights* blocks;  /* HOST array of `blocks` entries (device pointers inside) */
+} wan_dit_weights;
+
+/* Bytes of workspace wan_dit_forward / wan_dit_guided_step / wan_sample need. */
+size_t wan_dit_workspace_size(const wan_dit_config* cfg);
+
+/* [Method] + [Code]: the DiT velocity prediction.  patchify -> `blocks` transformer
+ * blocks (AdaLN-modulated self-attention with 3D RoPE, cross-attention to ctx_txt (and
+ * decoupled ctx_img), AdaLN-modulated GELU FFN, gated residuals) -> head -> depatchify.
+ * latent: fp32 [B, c_in, F, H, W], or [1, ...] broadcast to every batch entry when
+ * latent_broadcast != 0; t: fp32 [B] DEVICE timesteps in [0, 1]; ctx_txt: [B, Lt, D];
+ * ctx_img: [B, Li, D] or NULL (dtype); v_out: fp32 [B, c_out, F, H, W].
+ * ws: >= wan_dit_workspace_size(cfg) bytes, 1024-byte aligned. */
+int wan_dit_forward(const wan_dit_config* cfg, const wan_dit_weights* w, const float* latent,
+                    int latent_broadcast, const float* t, const void* ctx_txt, const void* ctx_img,
+                    float* v_out, void* ws, size_t ws_bytes, wan_stream_t stream);
+
+/* One guided denoising step (cfg->batch must be 2: cond, uncond).  Runs the DiT on
+ * [cond; uncond] with the shared latent x and timestep, then fuses CFG and the Euler
+ * update into x's first c_out channels.  x: fp32 [1, c_in, F, H, W] in/out;
+ * t_pair: fp32 DEVICE {t, t_next}; ctx_txt: [2, Lt, D] (cond first); ctx_img: [2, Li, D]
+ * or NULL.  v_ws: fp32 [2, c_out, F, H, W] receives the two velocity predictions. */
+int wan_dit_guided_step(const wan_dit_config* cfg, const wan_dit_weights* w, float* x,
+                        const float* t_pair, float guide_scale, const void* ctx_txt,
+                        const void* ctx_img, float* v_ws, void* ws, size_t ws_bytes,
+                        wan_stream_t stream);
+
+/* [Sampler 3.2, 4.4] End-to-end Euler sampling: `steps` guided steps on the uniform
+ * schedule t_k = 1 - k/steps, from noise x (t = 1) to the data estimate (t = 0).
+ * t_sched: fp32 DEVICE scratch of steps+1 floats; other arguments as for
+ * wan_dit_guided_step. */
+int wan_sample(const wan_dit_config* cfg, const wan_dit_weights* w, float* x, int steps,
+               float guide_scale, const void* ctx_txt, const void* ctx_img, float* t_sched,
+               float* v_ws, void* ws, size_t ws_bytes, wan_stream_t stream);
+
+/* ------------------------------------------------------------------ profiling
+ * Kernel timing with CUDA events recorded around every libwan launch while enabled.
+ * wan_profile_begin(capacity) starts recording (at most `capacity` launches);
+ * wan_profile_end(names, ms, counts, n_kinds) synchronises the recorded events and
+ * writes, per kernel kind, the total milliseconds and launch count; returns the number
+ * of kinds written (or a negative status).  names receives static strings. */
+int wan_profile_begin(int capacity);
+int wan_profile_end(const char** names, double* ms, int* counts, int max_kinds);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WAN_H_ */

@@ -240,7 +240,7 @@ def cross_attention(xr, blk, ctx_txt, ctx_img, hp):
     return linear(o.reshape(o.shape[0], D), blk["co_w"], blk["co_b"])
 
 
-def dit_block(x, mods, blk, ctx_txt, ctx_img, hp, rows=None):
+def dit_block(x, mods, blk, ctx_txt, ctx_img, hp, rows=None, trace=None):
     """One transformer block on one sample x [L, D].
 
     mods [6, D] = (shift1, scale1, gate1, shift2, scale2, gate2), the shared
@@ -250,7 +250,8 @@ def dit_block(x, mods, blk, ctx_txt, ctx_img, hp, rows=None):
 
     ``rows``: when given, only these output rows are produced.  Self-attention
     still sees every key and value; all later steps act row by row, so the result
-    equals the full block's rows.
+    equals the full block's rows.  ``trace``: optional dict that receives the
+    intermediate values at those rows.
     """
     D, H = hp.dim, hp.heads
     x = np.asarray(x, f64)
@@ -269,11 +270,17 @@ def dit_block(x, mods, blk, ctx_txt, ctx_img, hp, rows=None):
     q = rope3d(heads(linear(y[rows], wq, bq), H), pos[rows], hp.theta)
     o = attention(q, k, v).reshape(len(rows), D)
     xr = x[rows] + g1 * linear(o, blk["o_w"], blk["o_b"])
+    if trace is not None:
+        trace.update(y1=y[rows], q=q.reshape(len(rows), D), k=k[rows].reshape(len(rows), D),
+                     v=v[rows].reshape(len(rows), D), attn=o, x_sa=xr)
 
     xr = xr + cross_attention(xr, blk, ctx_txt, ctx_img, hp)
 
     y2 = modulate(layer_norm(xr, hp.eps), sh2, sc2)
-    xr = xr + g2 * linear(gelu(linear(y2, blk["f1_w"], blk["f1_b"])), blk["f2_w"], blk["f2_b"])
+    h = gelu(linear(y2, blk["f1_w"], blk["f1_b"]))
+    if trace is not None:
+        trace.update(x_ca=xr, y2=y2)
+    xr = xr + g2 * linear(h, blk["f2_w"], blk["f2_b"])
     return xr
 
 
@@ -289,7 +296,7 @@ def text_projection(text, w):
     return linear(gelu(linear(text, w["txt1_w"], w["txt1_b"])), w["txt2_w"], w["txt2_b"])
 
 
-def dit_forward(latent, t, ctx_txt, ctx_img, w, shape, rows=None, on_block=None):
+def dit_forward(latent, t, ctx_txt, ctx_img, w, shape, rows=None, on_block=None, trace=None):
     """The DiT's velocity prediction v [B, C_out, F, H, W] for latent [B, C_in, F, H, W],
     timesteps t [B] and contexts ctx_txt [B, Lt, D] (ctx_img [B, Li, D] or None).
 
@@ -308,7 +315,11 @@ def dit_forward(latent, t, ctx_txt, ctx_img, w, shape, rows=None, on_block=None)
         for b in range(B):
             blk = w["blocks"][0]
             ci = None if ctx_img is None else ctx_img[b]
-            xr = dit_block(x[b], e0[b] + blk["mod"], blk, ctx_txt[b], ci, hp, rows=rows)
+            tr = None if trace is None else {}
+            xr = dit_block(x[b], e0[b] + blk["mod"], blk, ctx_txt[b], ci, hp, rows=rows, trace=tr)
+            if trace is not None:
+                tr["x0"] = x[b][rows]
+                trace.setdefault("per_batch", []).append(tr)
             xs.append(xr)
             outs.append(head(xr, hm[b], w, shape.eps))
         return np.stack(outs), np.stack(xs)

@@ -1,0 +1,91 @@
+"""CPU checks of the C ABI boundary: the library loads without a GPU, exports every
+entry point include/wan.h declares, and its host-side validation and workspace
+arithmetic behave as documented (no kernel is launched here)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wan.h")
+LIB = os.path.join(ROOT, "video_diffusion_transformer_04_b300", "libwan.so")
+
+
+def declared():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(wan_[a-z0-9_]+)\s*\(", txt)))
+
+
+@pytest.fixture(scope="module")
+def wanlib():
+    if not os.path.exists(LIB):
+        from video_diffusion_transformer_04_b300 import _build
+        _build.build()
+    return C.CDLL(LIB)
+
+
+def test_header_declares_the_seven_step_entry_points():
+    names = declared()
+    for n in ("wan_patchify", "wan_adaln_modulate", "wan_attn_rope3d", "wan_cross_attn", "wan_ffn",
+              "wan_cfg_euler_step", "wan_dit_forward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(wanlib):
+    missing = [n for n in declared() if not hasattr(wanlib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol():
+    from video_diffusion_transformer_04_b300 import wan
+    assert sorted(wan.EXPORTED) == declared()
+
+
+def test_library_has_no_driver_link_dependency():
+    # The .so must load on a host without libcuda (the CPU suite runs without one).
+    import subprocess
+    out = subprocess.run(["ldd", LIB], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out and "libcudart.so" not in out
+
+
+def test_status_strings(wanlib):
+    wanlib.wan_status_string.restype = C.c_char_p
+    assert wanlib.wan_status_string(0) == b"ok"
+    assert b"timed out" in wanlib.wan_status_string(-4)
+    assert wanlib.wan_status_string(-99) == b"unknown status"
+
+
+def test_host_validation_rejects_bad_arguments(wanlib):
+    # Rejected before any CUDA call: NULL pointers, negative sizes, bad dtypes.
+    f = wanlib.wan_cfg_euler_step
+    f.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_longlong, C.c_float, C.c_float, C.c_int, C.c_void_p]
+    assert f(None, None, None, 0, 5.0, -0.05, 0, None) == 0          # n == 0 is a no-op
+    assert f(None, None, None, 16, 5.0, -0.05, 0, None) == -1       # NULL pointers
+    assert f(None, None, None, -1, 5.0, -0.05, 0, None) == -1       # negative n
+    assert f(None, None, None, 16, 5.0, -0.05, 7, None) == -1       # unknown dtype
+    g = wanlib.wan_linear
+    g.argtypes = [C.c_void_p] * 4 + [C.c_int] * 4 + [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p]
+    assert g(None, None, None, None, 8, 64, 64, 0, None, 0, 0, 0, None) == -1
+    assert g(None, None, None, None, 8, 64, 64, 9, None, 0, 0, 0, None) == -1
+
+
+def test_dit_workspace_size_arithmetic():
+    import synth
+    from video_diffusion_transformer_04_b300 import wan
+    s = synth.CONFIGS[2]
+    cfg = wan.wan_dit_config(dtype=wan.WAN_BF16, batch=2, c_in=16, c_out=16, frames=21, height=60, width=104,
+                             dim=1536, heads=12, head_dim=128, ffn=8960, blocks=30, text_len=512, img_len=0,
+                             freq_dim=256, theta=10000.0, eps=1e-6)
+    n = wan.wan_dit_workspace_size(cfg)
+    M, D = 2 * s.tokens, s.dim
+    # at least x (fp32), y, q|k, v^T, o, cross q and the FFN hidden (bf16)
+    lower = M * D * 4 + M * D * 2 * 5 + M * s.ffn * 2
+    assert lower <= n <= lower * 1.2
+    bad = wan.wan_dit_config(**{f: getattr(cfg, f) for f, _ in cfg._fields_})
+    bad.heads = 7
+    assert wan.wan_dit_workspace_size(bad) == 0
+    bad = wan.wan_dit_config(**{f: getattr(cfg, f) for f, _ in cfg._fields_})
+    bad.head_dim, bad.heads = 96, 16
+    assert wan.wan_dit_workspace_size(bad) == 0       # bf16 attention takes d = 64 or 128

@@ -1,0 +1,130 @@
+"""GPU parity of the whole DiT forward, guided step and sampler against the CPU fp64
+oracle on the benchmark workloads' seeded synthetic inputs.
+
+* the tiny configuration (fp32 and bf16) is compared element by element with the
+  oracle run live;
+* the full-size configurations are compared at the positions stored by
+  tests/golden/make_goldens.py (oracle output only).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import wan_oracle as O
+from tests.parity import assert_bf16_close, assert_f32_close, to_dev, to_np, tokens_of
+
+pytestmark = pytest.mark.gpu
+BF, F32 = torch.bfloat16, torch.float32
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _model(wan, s, seed=0):
+    w = synth.make_weights(s, seed)
+    inp = synth.make_inputs(s, seed)
+    return w, inp, wan.DiT(s, w)
+
+
+def _golden(n):
+    path = os.path.join(GOLDEN, f"config{n}.npz")
+    if not os.path.exists(path):
+        pytest.skip(f"{path} not generated")
+    return np.load(path)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tiny_guided_step(wan, dtype):
+    s = synth.CONFIGS[0].replace(dtype=dtype)
+    w, inp, m = _model(wan, s)
+    tdt = m.tdtype
+    ctx = m.text_embed(to_dev(inp["text"], tdt))
+    x = to_dev(inp["latent"], F32)
+    t = float(inp["t"][0])
+    t_pair = torch.tensor([t, t + s.dt], dtype=F32, device="cuda")
+    v = m.guided_step(x, t_pair, s.guide_scale, ctx)
+    wan.wan_sync_status()
+    ctx_o = O.text_projection(inp["text"], w)
+    lat2 = np.concatenate([inp["latent"]] * 2, axis=0)
+    v_o = O.dit_forward(lat2, np.array([t, t]), ctx_o, None, w, s)
+    dt = float(np.float32(t + s.dt)) - float(np.float32(t))
+    x_o = O.cfg_euler_step(inp["latent"], v_o[0:1], v_o[1:2], s.guide_scale, dt)
+    if dtype == "f32":
+        assert_f32_close(to_np(ctx), ctx_o, "ctx")
+        assert_f32_close(to_np(v), v_o, "v")
+        assert_f32_close(to_np(x), x_o, "x_next")
+    else:
+        assert_bf16_close(to_np(ctx), ctx_o, "ctx")
+        assert_bf16_close(to_np(v), v_o, "v")
+        assert_bf16_close(to_np(x) - inp["latent"], x_o - inp["latent"], "x_next - x")
+
+
+def test_tiny_forward_batch_permutation(wan):
+    # Permuting the batch (latents, timesteps, contexts) permutes the outputs.
+    s = synth.CONFIGS[0]
+    w, inp, m = _model(wan, s)
+    ctx = m.text_embed(to_dev(inp["text"], F32))
+    lat = torch.cat([to_dev(inp["latent"], F32), 0.5 * to_dev(inp["latent"], F32)])
+    t = torch.tensor([0.3, 0.8], dtype=F32, device="cuda")
+    v1 = m.forward(lat, t, ctx).clone()
+    v2 = m.forward(lat.flip(0).contiguous(), t.flip(0).contiguous(), ctx.flip(0).contiguous())
+    wan.wan_sync_status()
+    assert_f32_close(to_np(v2), to_np(v1)[::-1], "permuted batch", tol=1e-6)
+
+
+def _check_single_block(wan, n):
+    g = _golden(n)
+    s = synth.CONFIGS[n]
+    w, inp, m = _model(wan, s)
+    if s.text_dim:
+        ctx = m.text_embed(to_dev(inp["text"], BF))
+        assert_bf16_close(to_np(ctx[0])[g["ctx_rows"]], g["ctx"], "ctx rows")
+    else:
+        ctx = to_dev(inp["ctx_txt"], BF)
+    ctx_img = to_dev(inp["ctx_img"], BF) if s.img_len else None
+    v = m.forward(to_dev(inp["latent"], F32), to_dev(inp["t"], F32), ctx, ctx_img)
+    wan.wan_sync_status()
+    head = tokens_of(to_np(v))[0, g["rows"]]
+    assert_bf16_close(head, g["head"], f"config {n} head rows")
+
+
+def test_config1_block(wan):
+    _check_single_block(wan, 1)
+
+
+def test_config3_i2v_block(wan):
+    _check_single_block(wan, 3)
+
+
+def test_config2_guided_step(wan):
+    g = _golden(2)
+    s = synth.CONFIGS[2]
+    w, inp, m = _model(wan, s)
+    del w
+    ctx = m.text_embed(to_dev(inp["text"], BF))
+    x = to_dev(inp["latent"], F32)
+    t = float(inp["t"][0])
+    t_pair = torch.tensor([t, t + s.dt], dtype=F32, device="cuda")
+    v = m.guided_step(x, t_pair, s.guide_scale, ctx)
+    wan.wan_sync_status()
+    vt = tokens_of(to_np(v))
+    rows = g["rows"]
+    assert_bf16_close(vt[0, rows], g["v_cond"], "v_cond")
+    assert_bf16_close(vt[1, rows], g["v_uncond"], "v_uncond")
+    xt = tokens_of(to_np(x))[0, rows]
+    x0 = tokens_of(inp["latent"].astype(np.float64))[0, rows]
+    assert_bf16_close(xt - x0, g["x_next"] - x0, "x_next - x")
+
+
+def test_config4_sampler_shrunk(wan):
+    g = _golden(4)
+    Fr, H, W = (int(a) for a in g["shape"])
+    s = synth.CONFIGS[4].replace(frames=Fr, height=H, width=W)
+    w, inp, m = _model(wan, s)
+    del w
+    ctx = m.text_embed(to_dev(inp["text"], BF))
+    x = to_dev(inp["latent"], F32)
+    m.sample(x, s.steps, s.guide_scale, ctx)
+    wan.wan_sync_status()
+    assert_bf16_close(to_np(x), g["x_final"], "sampled x0")

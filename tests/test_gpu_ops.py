@@ -1,0 +1,258 @@
+"""GPU parity of each libwan entry point against the CPU fp64 oracle, at sizes that span
+several tiles plus ragged tails, and at the degenerate sizes (empty, one row, one key).
+Every call goes through the C ABI (video_diffusion_transformer_04_b300.wan)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import wan_oracle as O
+from tests.parity import assert_bf16_close, assert_f32_close, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+BF, F32 = torch.bfloat16, torch.float32
+
+
+def rb(a):
+    return synth.round_bf16(a)
+
+
+# ---------------------------------------------------------------- CFG + Euler
+
+@pytest.mark.parametrize("n", [0, 1, 7, 4099, 2096640])
+@pytest.mark.parametrize("vdt", ["f32", "bf16"])
+def test_cfg_euler(wan, n, vdt):
+    x = synth.normal(1, "cfg.x", (n,))
+    vc = synth.normal(1, "cfg.vc", (n,))
+    vu = synth.normal(1, "cfg.vu", (n,))
+    tdt = F32
+    if vdt == "bf16":
+        vc, vu, tdt = rb(vc), rb(vu), BF
+    xd = to_dev(x, F32)
+    wan.wan_cfg_euler_step(xd, to_dev(vc, tdt), to_dev(vu, tdt), 5.0, -0.05)
+    wan.wan_sync_status()
+    if n:
+        assert_f32_close(to_np(xd), O.cfg_euler_step(x, vc, vu, 5.0, np.float32(-0.05)), "cfg_euler", tol=1e-6)
+
+
+# ---------------------------------------------------------------- LayerNorm + AdaLN
+
+@pytest.mark.parametrize("B,L,D", [(2, 47, 128), (1, 300, 1536), (1, 129, 5120), (1, 1, 64)])
+@pytest.mark.parametrize("mod", [True, False])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_adaln_modulate(wan, B, L, D, mod, out):
+    x = synth.normal(2, "ln.x", (B, L, D)) * 2 + 0.5
+    sh = synth.normal(2, "ln.sh", (B, D)) * 0.3 if mod else None
+    sc = synth.normal(2, "ln.sc", (B, D)) * 0.3 if mod else None
+    y = torch.empty(B, L, D, dtype=BF if out == "bf16" else F32, device="cuda")
+    wan.wan_adaln_modulate(to_dev(x, F32), to_dev(sh, F32) if mod else None, to_dev(sc, F32) if mod else None, y)
+    wan.wan_sync_status()
+    ref = O.layer_norm(x, 1e-6)
+    if mod:
+        ref = O.modulate(ref, sh[:, None, :], sc[:, None, :])
+    if out == "bf16":
+        assert_bf16_close(to_np(y), ref, "adaln bf16")
+    else:
+        assert_f32_close(to_np(y), ref, "adaln f32", tol=2e-6)
+
+
+# ---------------------------------------------------------------- linear (tcgen05 GEMM core)
+
+LIN_CASES = [(1, 64, 64), (47, 96, 128), (128, 128, 64), (129, 256, 192), (300, 384, 1536), (1000, 1536, 512),
+             (257, 64, 4096), (130, 8960, 256)]
+
+
+@pytest.mark.parametrize("M,N,K", LIN_CASES)
+def test_linear_bf16_store_f32out(wan, M, N, K):
+    # bf16 inputs, fp32 output: only accumulation-order rounding remains, so a missing
+    # K slice, a wrong row/column or a swizzle mistake shows up at once.
+    x = rb(synth.normal(3, "lin.x", (M, K)))
+    w = rb(synth.normal(3, "lin.w", (N, K)) * 0.05)
+    b = rb(synth.normal(3, "lin.b", (N,)) * 0.02)
+    out = torch.full((M, N), float("nan"), dtype=F32, device="cuda")
+    wan.wan_linear(to_dev(x, BF), to_dev(w, BF), to_dev(b, BF), out, wan.WAN_EPI_STORE)
+    wan.wan_sync_status()
+    assert_f32_close(to_np(out), O.linear(x, w, b), f"linear {M}x{N}x{K}", tol=1e-4)
+
+
+@pytest.mark.parametrize("M,N,K", [(47, 96, 128), (300, 384, 1536), (130, 8960, 256)])
+@pytest.mark.parametrize("epi", ["store", "gelu", "resid"])
+def test_linear_bf16_epilogues(wan, M, N, K, epi):
+    x = rb(synth.normal(4, "lin.x", (M, K)))
+    w = rb(synth.normal(4, "lin.w", (N, K)) * 0.05)
+    b = rb(synth.normal(4, "lin.b", (N,)) * 0.02)
+    y = O.linear(x, w, b)
+    if epi == "resid":
+        rpg = max(1, M // 2)
+        x0 = synth.normal(4, "lin.x0", (M, N))
+        gate = synth.normal(4, "lin.g", ((M + rpg - 1) // rpg, N))
+        out = to_dev(x0, F32)
+        wan.wan_linear(to_dev(x, BF), to_dev(w, BF), to_dev(b, BF), out, wan.WAN_EPI_RESIDUAL, to_dev(gate, F32), rpg)
+        ref = x0 + gate[np.arange(M) // rpg] * y
+    else:
+        out = torch.empty((M, N), dtype=BF, device="cuda")
+        code = wan.WAN_EPI_STORE if epi == "store" else wan.WAN_EPI_GELU
+        wan.wan_linear(to_dev(x, BF), to_dev(w, BF), to_dev(b, BF), out, code)
+        ref = y if epi == "store" else O.gelu(y)
+    wan.wan_sync_status()
+    assert_bf16_close(to_np(out), ref, f"linear {epi}")
+
+
+@pytest.mark.parametrize("M,N,K", [(47, 96, 128), (130, 512, 256)])
+def test_linear_f32(wan, M, N, K):
+    x = synth.normal(5, "lin.x", (M, K))
+    w = synth.normal(5, "lin.w", (N, K)) * 0.05
+    b = synth.normal(5, "lin.b", (N,)) * 0.02
+    out = torch.empty((M, N), dtype=F32, device="cuda")
+    wan.wan_linear(to_dev(x, F32), to_dev(w, F32), to_dev(b, F32), out, wan.WAN_EPI_GELU)
+    wan.wan_sync_status()
+    assert_f32_close(to_np(out), O.gelu(O.linear(x, w, b)), "linear f32")
+
+
+# ---------------------------------------------------------------- self-attention with 3D RoPE
+
+ATTN_CASES = [  # (B, grid, H, d)
+    (1, (1, 1, 1), 1, 128),
+    (2, (3, 4, 4), 2, 64),
+    (1, (2, 5, 13), 2, 128),
+    (1, (1, 4, 64), 3, 128),
+    (2, (4, 9, 10), 2, 128),
+    (1, (3, 8, 27), 1, 64),
+]
+
+
+def _attn_inputs(seed, B, L, H, d, bf):
+    q = synth.normal(seed, "at.q", (B, L, H, d))
+    k = synth.normal(seed, "at.k", (B, L, H, d))
+    v = synth.normal(seed, "at.v", (B, L, H, d))
+    if bf:
+        q, k, v = rb(q), rb(k), rb(v)
+    return q, k, v
+
+
+@pytest.mark.parametrize("B,grid,H,d", ATTN_CASES)
+@pytest.mark.parametrize("rope", [True, False])
+def test_attn_rope3d_bf16(wan, B, grid, H, d, rope):
+    L = grid[0] * grid[1] * grid[2]
+    q, k, v = _attn_inputs(6, B, L, H, d, True)     # q, k ~ N(0, 1): peaky softmax
+    o = torch.full((B, L, H, d), float("nan"), dtype=BF, device="cuda")
+    ws = torch.empty(wan.wan_attn_workspace_size(B, L, H, d, wan.WAN_BF16) + 1024, dtype=torch.uint8, device="cuda")
+    ws = ws[(-ws.data_ptr()) % 1024:]
+    wan.wan_attn_rope3d(to_dev(q, BF), to_dev(k, BF), to_dev(v, BF), o, grid, apply_rope=rope, ws=ws)
+    wan.wan_sync_status()
+    pos = O.token_positions(grid)
+    for b in range(B):
+        qq = O.rope3d(q[b], pos) if rope else q[b]
+        kk = O.rope3d(k[b], pos) if rope else k[b]
+        assert_bf16_close(to_np(o[b]), O.attention(qq, kk, v[b]), f"attn b={b}")
+
+
+def test_attn_rope3d_f32(wan):
+    B, grid, H, d = 2, (3, 4, 5), 2, 64
+    L = 60
+    q, k, v = _attn_inputs(7, B, L, H, d, False)
+    o = torch.empty((B, L, H, d), dtype=F32, device="cuda")
+    ws = torch.empty(wan.wan_attn_workspace_size(B, L, H, d, wan.WAN_F32) + 1024, dtype=torch.uint8, device="cuda")
+    ws = ws[(-ws.data_ptr()) % 1024:]
+    wan.wan_attn_rope3d(to_dev(q, F32), to_dev(k, F32), to_dev(v, F32), o, grid, ws=ws)
+    wan.wan_sync_status()
+    pos = O.token_positions(grid)
+    for b in range(B):
+        assert_f32_close(to_np(o[b]), O.attention(O.rope3d(q[b], pos), O.rope3d(k[b], pos), v[b]), "attn f32")
+
+
+def test_attn_full_size_sampled_rows(wan):
+    # The 1.3B self-attention shape (32760 tokens, 12 heads of 128) checked on sampled
+    # query rows; every row sees all keys, so the sample is exact.
+    grid, H, d = (21, 30, 52), 12, 128
+    L = 32760
+    q, k, v = _attn_inputs(8, 1, L, H, d, True)
+    o = torch.empty((1, L, H, d), dtype=BF, device="cuda")
+    ws = torch.empty(wan.wan_attn_workspace_size(1, L, H, d, wan.WAN_BF16) + 1024, dtype=torch.uint8, device="cuda")
+    ws = ws[(-ws.data_ptr()) % 1024:]
+    wan.wan_attn_rope3d(to_dev(q, BF), to_dev(k, BF), to_dev(v, BF), o, grid, ws=ws)
+    wan.wan_sync_status()
+    rows = synth.sample_rows(L, 256, 8)
+    pos = O.token_positions(grid)
+    ref = O.attention(O.rope3d(q[0, rows], pos[rows]), O.rope3d(k[0], pos), v[0])
+    assert_bf16_close(to_np(o[0, rows]), ref, "attn full-size")
+
+
+# ---------------------------------------------------------------- cross-attention
+
+@pytest.mark.parametrize("B,L,Lt,Li,H,d", [(2, 130, 512, 257, 2, 128), (1, 48, 16, 0, 2, 64), (1, 1, 1, 1, 1, 128)])
+def test_cross_attn_bf16(wan, B, L, Lt, Li, H, d):
+    q = rb(synth.normal(9, "ca.q", (B, L, H, d)))
+    kt = rb(synth.normal(9, "ca.kt", (B, Lt, H, d)))
+    vt = rb(synth.normal(9, "ca.vt", (B, Lt, H, d)))
+    ki = rb(synth.normal(9, "ca.ki", (B, max(Li, 1), H, d)))[:, :Li]
+    vi = rb(synth.normal(9, "ca.vi", (B, max(Li, 1), H, d)))[:, :Li]
+    o = torch.full((B, L, H, d), float("nan"), dtype=BF, device="cuda")
+    ws = torch.empty(wan.wan_cross_attn_workspace_size(B, Lt, Li, H, d, wan.WAN_BF16) + 1024, dtype=torch.uint8,
+                     device="cuda")
+    ws = ws[(-ws.data_ptr()) % 1024:]
+    wan.wan_cross_attn(to_dev(q, BF), to_dev(kt, BF), to_dev(vt, BF), to_dev(ki, BF) if Li else None,
+                       to_dev(vi, BF) if Li else None, o, ws)
+    wan.wan_sync_status()
+    for b in range(B):
+        ref = O.attention(q[b], kt[b], vt[b])
+        if Li:
+            ref = ref + O.attention(q[b], ki[b], vi[b])
+        assert_bf16_close(to_np(o[b]), ref, "cross attn")
+
+
+# ---------------------------------------------------------------- patchify
+
+@pytest.mark.parametrize("B,C,Fr,H,W,D", [(1, 16, 3, 8, 8, 128), (1, 36, 2, 6, 10, 256), (2, 16, 1, 2, 2, 64)])
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_patchify(wan, B, C, Fr, H, W, D, dt):
+    lat = synth.normal(10, "pt.lat", (B, C, Fr, H, W))
+    w = synth.normal(10, "pt.w", (D, C * 4)) * 0.02
+    b = synth.normal(10, "pt.b", (D,)) * 0.02
+    tdt = F32
+    if dt == "bf16":
+        w, b, tdt = rb(w), rb(b), BF
+    L = Fr * (H // 2) * (W // 2)
+    x = torch.empty(B, L, D, dtype=F32, device="cuda")
+    ws = torch.empty(wan.wan_patchify_workspace_size(B, C, Fr, H, W, wan.dtype_code(tdt)), dtype=torch.uint8,
+                     device="cuda")
+    wan.wan_patchify(to_dev(lat, F32), to_dev(w, tdt), to_dev(b, tdt), x, ws)
+    wan.wan_sync_status()
+    # the bf16 path keeps the fp32 latent exactly (two-term bf16 split), so it meets the
+    # fp32 bound too
+    assert_f32_close(to_np(x), O.patchify(lat, w, b), "patchify", tol=1e-4)
+
+
+# ---------------------------------------------------------------- FFN
+
+@pytest.mark.parametrize("B,L,D,Fh", [(2, 100, 128, 512), (1, 257, 1536, 8960)])
+def test_ffn_bf16(wan, B, L, D, Fh):
+    y = rb(synth.normal(11, "ffn.y", (B, L, D)))
+    w1 = rb(synth.normal(11, "ffn.w1", (Fh, D)) * 0.02)
+    b1 = rb(synth.normal(11, "ffn.b1", (Fh,)) * 0.02)
+    w2 = rb(synth.normal(11, "ffn.w2", (D, Fh)) * 0.02)
+    b2 = rb(synth.normal(11, "ffn.b2", (D,)) * 0.02)
+    gate = synth.normal(11, "ffn.g", (B, D))
+    x0 = synth.normal(11, "ffn.x", (B, L, D))
+    x = to_dev(x0, F32)
+    h = torch.empty(B, L, Fh, dtype=BF, device="cuda")
+    wan.wan_ffn(to_dev(y, BF), to_dev(w1, BF), to_dev(b1, BF), to_dev(w2, BF), to_dev(b2, BF), to_dev(gate, F32), x, h)
+    wan.wan_sync_status()
+    delta = O.linear(O.gelu(O.linear(y, w1, b1)), w2, b2)
+    ref = x0 + gate[:, None, :] * delta
+    assert_bf16_close(to_np(x) - x0, ref - x0, "ffn residual update")
+
+
+# ---------------------------------------------------------------- text projection
+
+@pytest.mark.parametrize("B,Lt,Ct,D", [(2, 16, 128, 128), (1, 512, 4096, 1536)])
+def test_text_embed(wan, B, Lt, Ct, D):
+    text = rb(synth.normal(12, "te.x", (B, Lt, Ct)))
+    w = {"txt1_w": rb(synth.normal(12, "te.w1", (D, Ct)) * 0.02), "txt1_b": rb(synth.normal(12, "te.b1", (D,)) * 0.02),
+         "txt2_w": rb(synth.normal(12, "te.w2", (D, D)) * 0.02), "txt2_b": rb(synth.normal(12, "te.b2", (D,)) * 0.02)}
+    ctx = torch.empty(B, Lt, D, dtype=BF, device="cuda")
+    ws = torch.empty(wan.wan_text_embed_workspace_size(B, Lt, D, wan.WAN_BF16), dtype=torch.uint8, device="cuda")
+    wan.wan_text_embed(to_dev(text, BF), *(to_dev(w[k], BF) for k in ("txt1_w", "txt1_b", "txt2_w", "txt2_b")), ctx,
+                       ws)
+    wan.wan_sync_status()
+    assert_bf16_close(to_np(ctx), O.text_projection(text, w), "text embed")

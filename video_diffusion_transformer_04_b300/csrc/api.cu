@@ -1,0 +1,760 @@
+// C ABI of libwan (include/wan.h): argument validation, tensor-map creation, workspace
+// planning, the orchestration of the DiT forward / guided step / sampler, and the
+// launch counter and event profiler.  No entry point allocates device memory.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+
+// Device status word (per device context): kernels record pipeline-wait timeouts here.
+__device__ int g_wan_status = 0;
+
+namespace wan {
+
+// ------------------------------------------------------------------ launch bookkeeping
+static std::atomic<long long> g_launches{0};
+
+struct ProfRec {
+  const char* kind;
+  cudaEvent_t a, b;
+};
+static std::mutex g_prof_mu;
+static bool g_prof_on = false;
+static bool g_prof_open = false;
+static std::vector<ProfRec> g_recs;
+static std::vector<cudaEvent_t> g_pool;
+static size_t g_cap = 0;
+
+void count_launch(const char* kind, cudaStream_t stream, bool begin) {
+  if (begin) g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (!g_prof_on) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (begin) {
+    g_prof_open = false;
+    if (g_recs.size() < g_cap) {
+      const size_t i = g_recs.size();
+      ProfRec r{kind, g_pool[2 * i], g_pool[2 * i + 1]};
+      if (cudaEventRecord(r.a, stream) == cudaSuccess) {
+        g_recs.push_back(r);
+        g_prof_open = true;
+      }
+    }
+  } else if (g_prof_open) {
+    cudaEventRecord(g_recs.back().b, stream);
+    g_prof_open = false;
+  }
+}
+
+struct DevInfo {
+  int* status = nullptr;
+  int num_sms = 0;
+};
+static std::mutex g_dev_mu;
+static DevInfo g_dev[64];
+
+int launch_ctx(cudaStream_t stream, LaunchCtx* ctx) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WAN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.status) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_wan_status) != cudaSuccess) return WAN_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return WAN_ERR_CUDA;
+    d.status = static_cast<int*>(p);
+    d.num_sms = sms;
+  }
+  ctx->stream = stream;
+  ctx->dev_status = d.status;
+  ctx->num_sms = d.num_sms;
+  return WAN_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int make_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t d0, uint64_t d1,
+                 uint64_t stride1_bytes, uint32_t box0, uint32_t box1) {
+  auto enc = encoder();
+  if (!enc) return WAN_ERR_CUDA;
+  if (!aligned16(base) || stride1_bytes % 16 != 0 || box0 * (uint32_t)elem_bytes != 128) return WAN_ERR_UNSUPPORTED;
+  cuuint64_t dims[2] = {d0, d1};
+  cuuint64_t strides[1] = {stride1_bytes};
+  cuuint32_t box[2] = {box0, box1};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? WAN_OK : WAN_ERR_UNSUPPORTED;
+}
+
+int make_tmap_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t d0, uint64_t d1,
+                 uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1) {
+  auto enc = encoder();
+  if (!enc) return WAN_ERR_CUDA;
+  if (!aligned16(base) || stride1_bytes % 16 != 0 || stride2_bytes % 16 != 0 || box0 * (uint32_t)elem_bytes != 128)
+    return WAN_ERR_UNSUPPORTED;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? WAN_OK : WAN_ERR_UNSUPPORTED;
+}
+
+// ------------------------------------------------------------------ helpers
+#define WAN_TRY(expr)          \
+  do {                         \
+    const int _st = (expr);    \
+    if (_st != WAN_OK) return _st; \
+  } while (0)
+
+static inline long long round_up(long long v, long long a) { return (v + a - 1) / a * a; }
+
+struct Bump {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Bump(void* b) : base(static_cast<uint8_t*>(b)) {}
+  template <typename T>
+  T* take(size_t count, size_t elem = sizeof(T)) {
+    off = (size_t)round_up((long long)off, 1024);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * elem;
+    return p;
+  }
+};
+
+static EpiParams epi_base(int kind, int M, int N, int rows_per_batch, const void* bias, int f32) {
+  EpiParams e;
+  memset(&e, 0, sizeof(e));
+  e.kind = kind;
+  e.M = M;
+  e.N = N;
+  e.rows_per_batch = rows_per_batch > 0 ? rows_per_batch : (M > 0 ? M : 1);
+  e.bias = bias;
+  e.bias_f32 = f32;
+  return e;
+}
+
+// y = A W^T (+ epilogue) in the call's dtype.
+static int proj(const LaunchCtx& c, int f32, const void* A, long long lda, int a_cols, const void* W, long long ldw,
+                int w_cols, int M, int N, int K, int kb_period, const EpiParams& ep, const char* tag) {
+  if (f32) return gemm_f32(c, static_cast<const float*>(A), lda, static_cast<const float*>(W), ldw, M, N, K, ep, tag);
+  return gemm_bf16(c, static_cast<const bf16*>(A), lda, a_cols, static_cast<const bf16*>(W), ldw, w_cols, M, N, K,
+                   kb_period, ep, tag);
+}
+
+static int attend(const LaunchCtx& c, int f32, const AttnArgs& a) {
+  return f32 ? attention_f32(c, a) : attention_bf16(c, a);
+}
+
+static int check_dtype(int dtype) { return (dtype == WAN_BF16 || dtype == WAN_F32) ? WAN_OK : WAN_ERR_INVALID_ARG; }
+
+// ------------------------------------------------------------------ patchify
+static long long patch_kpad(int C, int f32) { return f32 ? 4LL * C : round_up(4LL * C, 64); }
+
+static size_t patch_ws_bytes(int B, int C, int F, int H, int W, int f32) {
+  const long long M = (long long)B * F * (H / 2) * (W / 2);
+  return f32 ? (size_t)(M * 4 * C * 4) : (size_t)(M * 2 * patch_kpad(C, 0) * 2);
+}
+
+static int patchify_impl(const LaunchCtx& c, const float* latent, long long lat_bstride, const void* w, const void* b,
+                         float* x, int B, int C, int F, int H, int W, int D, int f32, void* A) {
+  const int L = F * (H / 2) * (W / 2);
+  const int M = B * L;
+  const long long kpad = patch_kpad(C, f32);
+  WAN_TRY(launch_patch_gather(c, latent, lat_bstride, A, f32, B, C, F, H, W, (int)kpad));
+  EpiParams ep = epi_base(EPI_STORE, M, D, L, b, f32);
+  ep.out = x;
+  ep.ldo = D;
+  ep.out_f32 = 1;
+  if (f32) return proj(c, 1, A, 4LL * C, 4 * C, w, 4LL * C, 4 * C, M, D, 4 * C, 0, ep, "gemm_patchify");
+  return proj(c, 0, A, 2 * kpad, (int)(2 * kpad), w, 4LL * C, 4 * C, M, D, (int)(2 * kpad), (int)(kpad / 64), ep,
+              "gemm_patchify");
+}
+
+// ------------------------------------------------------------------ forward workspace plan
+struct FwdWs {
+  float* x;
+  void *y, *qk, *vt, *o, *qc, *kc, *vct, *kci, *vcit, *h, *patchA;
+  float *tsin, *h1, *e, *e0, *hm, *mods;
+  float2* rope;
+  size_t bytes;
+};
+
+static long long vt_ld(int L) { return round_up(L, 8); }
+
+static FwdWs plan_forward(const wan_dit_config* cfg, void* ws) {
+  const int f32 = cfg->dtype == WAN_F32;
+  const size_t es = f32 ? 4 : 2;
+  const long long B = cfg->batch, D = cfg->dim, H = cfg->heads, hd = cfg->head_dim;
+  const long long L = (long long)cfg->frames * (cfg->height / 2) * (cfg->width / 2);
+  const long long M = B * L;
+  Bump bp(ws);
+  FwdWs w;
+  w.x = bp.take<float>(M * D);
+  w.y = bp.take<uint8_t>(M * D * es);
+  w.qk = bp.take<uint8_t>(M * 2 * D * es);
+  w.vt = bp.take<uint8_t>(B * H * hd * vt_ld((int)L) * es);
+  w.o = bp.take<uint8_t>(M * D * es);
+  w.qc = bp.take<uint8_t>(M * D * es);
+  w.kc = bp.take<uint8_t>(B * cfg->text_len * D * es);
+  w.vct = bp.take<uint8_t>(B * H * hd * vt_ld(cfg->text_len) * es);
+  w.kci = cfg->img_len ? bp.take<uint8_t>(B * cfg->img_len * D * es) : nullptr;
+  w.vcit = cfg->img_len ? bp.take<uint8_t>(B * H * hd * vt_ld(cfg->img_len) * es) : nullptr;
+  w.h = bp.take<uint8_t>(M * (long long)cfg->ffn * es);
+  w.patchA = bp.take<uint8_t>(patch_ws_bytes((int)B, cfg->c_in, cfg->frames, cfg->height, cfg->width, f32));
+  w.tsin = bp.take<float>(B * cfg->freq_dim);
+  w.h1 = bp.take<float>(B * D);
+  w.e = bp.take<float>(B * D);
+  w.e0 = bp.take<float>(B * 6 * D);
+  w.hm = bp.take<float>(B * 2 * D);
+  w.mods = bp.take<float>((long long)cfg->blocks * B * 6 * D);
+  w.rope = bp.take<float2>(rope_table_entries(cfg->frames, cfg->height / 2, cfg->width / 2, (int)hd));
+  w.bytes = (size_t)round_up((long long)bp.off, 1024);
+  return w;
+}
+
+static int validate_cfg(const wan_dit_config* cfg) {
+  if (!cfg) return WAN_ERR_INVALID_ARG;
+  WAN_TRY(check_dtype(cfg->dtype));
+  if (cfg->batch <= 0 || cfg->c_in <= 0 || cfg->c_out <= 0 || cfg->frames <= 0 || cfg->height <= 0 ||
+      cfg->width <= 0 || cfg->dim <= 0 || cfg->heads <= 0 || cfg->head_dim <= 0 || cfg->ffn <= 0 ||
+      cfg->blocks <= 0 || cfg->text_len <= 0 || cfg->img_len < 0 || cfg->freq_dim <= 0 || cfg->freq_dim % 2)
+    return WAN_ERR_INVALID_ARG;
+  if (cfg->height % 2 || cfg->width % 2 || cfg->heads * cfg->head_dim != cfg->dim) return WAN_ERR_INVALID_ARG;
+  if (cfg->dim % 32 || cfg->ffn % 32 || cfg->c_out * 4 % 32 || cfg->dim > 8192) return WAN_ERR_UNSUPPORTED;
+  if (cfg->dtype == WAN_BF16 && cfg->head_dim != 64 && cfg->head_dim != 128) return WAN_ERR_UNSUPPORTED;
+  if (cfg->dtype == WAN_F32 && (cfg->head_dim > 128 || cfg->head_dim % 2)) return WAN_ERR_UNSUPPORTED;
+  if (cfg->freq_dim % 8) return WAN_ERR_UNSUPPORTED;
+  return WAN_OK;
+}
+
+static int validate_weights(const wan_dit_config* cfg, const wan_dit_weights* w) {
+  if (!w || !w->blocks) return WAN_ERR_INVALID_ARG;
+  const void* g[] = {w->patch_w, w->patch_b, w->t1_w, w->t1_b, w->t2_w, w->t2_b, w->m_w,
+                     w->m_b,     w->hm_w,    w->hm_b, w->head_w, w->head_b};
+  for (const void* p : g)
+    if (!p || !aligned16(p)) return WAN_ERR_INVALID_ARG;
+  for (int i = 0; i < cfg->blocks; ++i) {
+    const wan_block_weights& b = w->blocks[i];
+    const void* q[] = {b.mod, b.qkv_w, b.qkv_b, b.o_w, b.o_b, b.cq_w, b.cq_b, b.ckv_w,
+                       b.ckv_b, b.co_w, b.co_b, b.f1_w, b.f1_b, b.f2_w, b.f2_b};
+    for (const void* p : q)
+      if (!p || !aligned16(p)) return WAN_ERR_INVALID_ARG;
+    if (cfg->img_len && (!b.ckvi_w || !b.ckvi_b)) return WAN_ERR_INVALID_ARG;
+  }
+  return WAN_OK;
+}
+
+static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w, const float* latent,
+                            long long lat_bstride, const float* t, int t_stride, const void* ctx_txt,
+                            const void* ctx_img, float* v_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  WAN_TRY(validate_cfg(cfg));
+  WAN_TRY(validate_weights(cfg, w));
+  if (!latent || !t || !ctx_txt || !v_out || (cfg->img_len && !ctx_img)) return WAN_ERR_INVALID_ARG;
+  if (!aligned16(latent) || !aligned16(ctx_txt) || !aligned16(v_out) || (ctx_img && !aligned16(ctx_img)))
+    return WAN_ERR_UNSUPPORTED;
+  FwdWs W = plan_forward(cfg, nullptr);
+  if (!ws || ws_bytes < W.bytes || (reinterpret_cast<uintptr_t>(ws) & 1023)) return WAN_ERR_WORKSPACE;
+  W = plan_forward(cfg, ws);
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+
+  const int f32 = cfg->dtype == WAN_F32;
+  const int B = cfg->batch, D = cfg->dim, H = cfg->heads, hd = cfg->head_dim, Fh = cfg->ffn;
+  const int Lt = cfg->text_len, Li = cfg->img_len;
+  const int Fg = cfg->frames, Hg = cfg->height / 2, Wg = cfg->width / 2;
+  const int L = Fg * Hg * Wg;
+  const int M = B * L;
+
+  // 3D RoPE table and the shared time embedding -> six modulation vectors per block.
+  WAN_TRY(launch_rope_table(c, W.rope, Fg, Hg, Wg, hd, cfg->theta));
+  const RopeGeom rg = rope_geom(W.rope, Fg, Hg, Wg, hd);
+  WAN_TRY(launch_sinusoid(c, t, t_stride, W.tsin, B, cfg->freq_dim));
+  WAN_TRY(launch_small_linear(c, W.tsin, w->t1_w, w->t1_b, f32, W.h1, B, D, cfg->freq_dim, 0, 1));
+  WAN_TRY(launch_small_linear(c, W.h1, w->t2_w, w->t2_b, f32, W.e, B, D, D, 0, 0));
+  WAN_TRY(launch_small_linear(c, W.e, w->m_w, w->m_b, f32, W.e0, B, 6 * D, D, 1, 0));
+  WAN_TRY(launch_small_linear(c, W.e, w->hm_w, w->hm_b, f32, W.hm, B, 2 * D, D, 1, 0));
+  {
+    std::vector<const void*> mp(cfg->blocks);
+    for (int i = 0; i < cfg->blocks; ++i) mp[i] = w->blocks[i].mod;
+    WAN_TRY(launch_block_mods(c, W.e0, mp.data(), cfg->blocks, f32, W.mods, B, D));
+  }
+
+  WAN_TRY(patchify_impl(c, latent, lat_bstride, w->patch_w, w->patch_b, W.x, B, cfg->c_in, cfg->frames,
+                        cfg->height, cfg->width, D, f32, W.patchA));
+
+  const long long ldvt = vt_ld(L), ldvc = vt_ld(Lt), ldvi = vt_ld(Li > 0 ? Li : 1);
+  for (int i = 0; i < cfg->blocks; ++i) {
+    const wan_block_weights& bw = w->blocks[i];
+    const float* mod = W.mods + (long long)i * B * 6 * D;  // [B][6][D]
+
+    // --- self-attention: y = LN(x)(1+sc1)+sh1; q,k (RoPE), v^T; attention; x += g1 (o Wo^T + bo)
+    WAN_TRY(launch_ln_mod(c, W.x, mod + 0 * D, mod + 1 * D, 6LL * D, W.y, f32, M, L, D, cfg->eps));
+    {
+      EpiParams ep = epi_base(EPI_QKV, M, 3 * D, L, bw.qkv_b, f32);
+      ep.qk = W.qk;
+      ep.ldqk = 2LL * D;
+      ep.qk_f32 = f32;
+      ep.n_qk = 2 * D;
+      ep.n_rot = 2 * D;
+      ep.vt = W.vt;
+      ep.ld_vt = ldvt;
+      ep.head_dim = hd;
+      ep.heads = H;
+      ep.rope = rg;
+      WAN_TRY(proj(c, f32, W.y, D, D, bw.qkv_w, D, D, M, 3 * D, D, 0, ep, "gemm_qkv_rope"));
+    }
+    {
+      AttnArgs a;
+      memset(&a, 0, sizeof(a));
+      a.q = W.qk; a.ldq = 2LL * D; a.q_row_len = 2 * D; a.q_col = 0;
+      a.k = W.qk; a.ldk = 2LL * D; a.k_row_len = 2 * D; a.k_col = D;
+      a.vt = W.vt; a.ld_vt = ldvt;
+      a.o = W.o; a.ldo = D; a.o_col = 0;
+      a.B = B; a.Lq = L; a.Lkv = L; a.H = H; a.head_dim = hd;
+      a.tag = "attn_self";
+      WAN_TRY(attend(c, f32, a));
+    }
+    {
+      EpiParams ep = epi_base(EPI_RESID, M, D, L, bw.o_b, f32);
+      ep.resid = W.x;
+      ep.ldr = D;
+      ep.gate = mod + 2 * D;
+      ep.ld_gate = 6LL * D;
+      WAN_TRY(proj(c, f32, W.o, D, D, bw.o_w, D, D, M, D, D, 0, ep, "gemm_o_gate"));
+    }
+
+    // --- cross-attention: q = LN(x) Wq^T; k,v from the context; x += o Wo^T + bo
+    WAN_TRY(launch_ln_mod(c, W.x, nullptr, nullptr, 0, W.y, f32, M, L, D, cfg->eps));
+    {
+      EpiParams ep = epi_base(EPI_STORE, M, D, L, bw.cq_b, f32);
+      ep.out = W.qc;
+      ep.ldo = D;
+      ep.out_f32 = f32;
+      WAN_TRY(proj(c, f32, W.y, D, D, bw.cq_w, D, D, M, D, D, 0, ep, "gemm_cross_q"));
+    }
+    for (int seg = 0; seg < (Li ? 2 : 1); ++seg) {
+      const int Lk = seg ? Li : Lt;
+      void* kbuf = seg ? W.kci : W.kc;
+      void* vbuf = seg ? W.vcit : W.vct;
+      const long long ldv = seg ? ldvi : ldvc;
+      EpiParams ep = epi_base(EPI_QKV, B * Lk, 2 * D, Lk, seg ? bw.ckvi_b : bw.ckv_b, f32);
+      ep.qk = kbuf;
+      ep.ldqk = D;
+      ep.qk_f32 = f32;
+      ep.n_qk = D;
+      ep.n_rot = 0;
+      ep.vt = vbuf;
+      ep.ld_vt = ldv;
+      ep.head_dim = hd;
+      ep.heads = H;
+      WAN_TRY(proj(c, f32, seg ? ctx_img : ctx_txt, D, D, seg ? bw.ckvi_w : bw.ckv_w, D, D, B * Lk, 2 * D, D, 0, ep,
+                   "gemm_cross_kv"));
+      AttnArgs a;
+      memset(&a, 0, sizeof(a));
+      a.q = W.qc; a.ldq = D; a.q_row_len = D; a.q_col = 0;
+      a.k = kbuf; a.ldk = D; a.k_row_len = D; a.k_col = 0;
+      a.vt = vbuf; a.ld_vt = ldv;
+      a.o = W.o; a.ldo = D; a.o_col = 0;
+      a.B = B; a.Lq = L; a.Lkv = Lk; a.H = H; a.head_dim = hd;
+      a.accumulate = seg;
+      a.tag = "attn_cross";
+      WAN_TRY(attend(c, f32, a));
+    }
+    {
+      EpiParams ep = epi_base(EPI_RESID, M, D, L, bw.co_b, f32);
+      ep.resid = W.x;
+      ep.ldr = D;
+      WAN_TRY(proj(c, f32, W.o, D, D, bw.co_w, D, D, M, D, D, 0, ep, "gemm_cross_o"));
+    }
+
+    // --- FFN: y = LN(x)(1+sc2)+sh2; h = GELU(y W1^T + b1); x += g2 (h W2^T + b2)
+    WAN_TRY(launch_ln_mod(c, W.x, mod + 3 * D, mod + 4 * D, 6LL * D, W.y, f32, M, L, D, cfg->eps));
+    {
+      EpiParams ep = epi_base(EPI_GELU, M, Fh, L, bw.f1_b, f32);
+      ep.out = W.h;
+      ep.ldo = Fh;
+      ep.out_f32 = f32;
+      WAN_TRY(proj(c, f32, W.y, D, D, bw.f1_w, D, D, M, Fh, D, 0, ep, "gemm_ffn1_gelu"));
+    }
+    {
+      EpiParams ep = epi_base(EPI_RESID, M, D, L, bw.f2_b, f32);
+      ep.resid = W.x;
+      ep.ldr = D;
+      ep.gate = mod + 5 * D;
+      ep.ld_gate = 6LL * D;
+      WAN_TRY(proj(c, f32, W.h, Fh, Fh, bw.f2_w, Fh, Fh, M, D, Fh, 0, ep, "gemm_ffn2_gate"));
+    }
+  }
+
+  // head: LN(x)(1+sc_h)+sh_h -> Linear D -> c_out*4 -> depatchify
+  WAN_TRY(launch_ln_mod(c, W.x, W.hm, W.hm + D, 2LL * D, W.y, f32, M, L, D, cfg->eps));
+  {
+    EpiParams ep = epi_base(EPI_HEAD, M, cfg->c_out * 4, L, w->head_b, f32);
+    ep.vout = v_out;
+    ep.C = cfg->c_out;
+    ep.F = cfg->frames;
+    ep.H = cfg->height;
+    ep.W = cfg->width;
+    WAN_TRY(proj(c, f32, W.y, D, D, w->head_w, D, D, M, cfg->c_out * 4, D, 0, ep, "gemm_head"));
+  }
+  return WAN_OK;
+}
+
+}  // namespace wan
+
+using namespace wan;
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char* wan_status_string(int status) {
+  switch (status) {
+    case WAN_OK: return "ok";
+    case WAN_ERR_INVALID_ARG: return "invalid argument";
+    case WAN_ERR_UNSUPPORTED: return "unsupported shape, alignment or dtype";
+    case WAN_ERR_CUDA: return "CUDA runtime error";
+    case WAN_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case WAN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+int wan_sync_status(wan_stream_t stream) {
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return WAN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, c.dev_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return WAN_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    cudaMemcpy(c.dev_status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    return WAN_ERR_TIMEOUT;
+  }
+  return WAN_OK;
+}
+
+long long wan_launch_count(void) { return g_launches.load(); }
+
+size_t wan_patchify_workspace_size(int B, int C, int F, int H, int W, int dtype) {
+  if (B <= 0 || C <= 0 || F <= 0 || H <= 0 || W <= 0) return 0;
+  return patch_ws_bytes(B, C, F, H, W, dtype == WAN_F32);
+}
+
+int wan_patchify(const float* latent, const void* w, const void* b, float* x, int B, int C, int F, int H, int W,
+                 int D, int dtype, void* ws, size_t ws_bytes, wan_stream_t stream) {
+  WAN_TRY(check_dtype(dtype));
+  if (!latent || !w || !b || !x || B <= 0 || C <= 0 || F <= 0 || H <= 0 || W <= 0 || D <= 0 || H % 2 || W % 2)
+    return WAN_ERR_INVALID_ARG;
+  if (D % 32 || !aligned16(latent) || !aligned16(w) || !aligned16(x)) return WAN_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < patch_ws_bytes(B, C, F, H, W, dtype == WAN_F32) || !aligned16(ws)) return WAN_ERR_WORKSPACE;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  return patchify_impl(c, latent, (long long)C * F * H * W, w, b, x, B, C, F, H, W, D, dtype == WAN_F32, ws);
+}
+
+int wan_adaln_modulate(const float* x, const float* shift, const float* scale, void* y, int B, int L, int D,
+                       float eps, int dtype, wan_stream_t stream) {
+  WAN_TRY(check_dtype(dtype));
+  if (!x || !y || B <= 0 || L <= 0 || D <= 0 || (!shift) != (!scale)) return WAN_ERR_INVALID_ARG;
+  if (D % 4 || D > 8192 || !aligned16(x) || !aligned16(y) || (shift && (!aligned16(shift) || !aligned16(scale))))
+    return WAN_ERR_UNSUPPORTED;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  return launch_ln_mod(c, x, shift, scale, D, y, dtype == WAN_F32, B * L, L, D, eps);
+}
+
+size_t wan_attn_workspace_size(int B, int L, int H, int d, int dtype) {
+  if (B <= 0 || L <= 0 || H <= 0 || d <= 0) return 0;
+  const size_t es = dtype == WAN_F32 ? 4 : 2;
+  Bump bp(nullptr);
+  bp.take<float2>((size_t)L * d);  // RoPE table (upper bound)
+  bp.take<uint8_t>((size_t)B * L * H * d * es);
+  bp.take<uint8_t>((size_t)B * L * H * d * es);
+  bp.take<uint8_t>((size_t)B * H * d * vt_ld(L) * es);
+  return (size_t)round_up((long long)bp.off, 1024);
+}
+
+int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B, int L, int H, int d, int Fg, int Hg,
+                    int Wg, float theta, int apply_rope, int dtype, void* ws, size_t ws_bytes, wan_stream_t stream) {
+  WAN_TRY(check_dtype(dtype));
+  const int f32 = dtype == WAN_F32;
+  if (!q || !k || !v || !o || B <= 0 || L <= 0 || H <= 0 || d <= 0) return WAN_ERR_INVALID_ARG;
+  if (apply_rope && (Fg <= 0 || Hg <= 0 || Wg <= 0 || (long long)Fg * Hg * Wg != L)) return WAN_ERR_INVALID_ARG;
+  if ((!f32 && d != 64 && d != 128) || (f32 && (d > 128 || d % 2))) return WAN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return WAN_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < wan_attn_workspace_size(B, L, H, d, dtype) || (reinterpret_cast<uintptr_t>(ws) & 1023))
+    return WAN_ERR_WORKSPACE;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  const size_t es = f32 ? 4 : 2;
+  Bump bp(ws);
+  float2* tab = bp.take<float2>((size_t)L * d);
+  void* qr = bp.take<uint8_t>((size_t)B * L * H * d * es);
+  void* kr = bp.take<uint8_t>((size_t)B * L * H * d * es);
+  void* vt = bp.take<uint8_t>((size_t)B * H * d * vt_ld(L) * es);
+  const void* qa = q;
+  const void* ka = k;
+  if (apply_rope) {
+    WAN_TRY(launch_rope_table(c, tab, Fg, Hg, Wg, d, theta));
+    const RopeGeom g = rope_geom(tab, Fg, Hg, Wg, d);
+    WAN_TRY(launch_rope_apply(c, q, qr, g, B, L, H, d, f32));
+    WAN_TRY(launch_rope_apply(c, k, kr, g, B, L, H, d, f32));
+    qa = qr;
+    ka = kr;
+  }
+  WAN_TRY(launch_transpose_v(c, v, vt, vt_ld(L), B, L, H, d, f32));
+  AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  const int D = H * d;
+  a.q = qa; a.ldq = D; a.q_row_len = D;
+  a.k = ka; a.ldk = D; a.k_row_len = D;
+  a.vt = vt; a.ld_vt = vt_ld(L);
+  a.o = o; a.ldo = D;
+  a.B = B; a.Lq = L; a.Lkv = L; a.H = H; a.head_dim = d;
+  a.tag = "attn_self";
+  return attend(c, f32, a);
+}
+
+size_t wan_cross_attn_workspace_size(int B, int Lt, int Li, int H, int d, int dtype) {
+  if (B <= 0 || Lt <= 0 || Li < 0 || H <= 0 || d <= 0) return 0;
+  const size_t es = dtype == WAN_F32 ? 4 : 2;
+  Bump bp(nullptr);
+  bp.take<uint8_t>((size_t)B * H * d * vt_ld(Lt) * es);
+  if (Li) bp.take<uint8_t>((size_t)B * H * d * vt_ld(Li) * es);
+  return (size_t)round_up((long long)bp.off, 1024);
+}
+
+int wan_cross_attn(const void* q, const void* kt, const void* vt, const void* ki, const void* vi, void* o, int B,
+                   int L, int Lt, int Li, int H, int d, int dtype, void* ws, size_t ws_bytes, wan_stream_t stream) {
+  WAN_TRY(check_dtype(dtype));
+  const int f32 = dtype == WAN_F32;
+  if (!q || !kt || !vt || !o || B <= 0 || L <= 0 || Lt <= 0 || Li < 0 || H <= 0 || d <= 0) return WAN_ERR_INVALID_ARG;
+  if (Li > 0 && (!ki || !vi)) return WAN_ERR_INVALID_ARG;
+  if ((!f32 && d != 64 && d != 128) || (f32 && (d > 128 || d % 2))) return WAN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(kt) || !aligned16(vt) || !aligned16(o) || (Li && (!aligned16(ki) || !aligned16(vi))))
+    return WAN_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < wan_cross_attn_workspace_size(B, Lt, Li, H, d, dtype) ||
+      (reinterpret_cast<uintptr_t>(ws) & 1023))
+    return WAN_ERR_WORKSPACE;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  const size_t es = f32 ? 4 : 2;
+  Bump bp(ws);
+  void* vtt = bp.take<uint8_t>((size_t)B * H * d * vt_ld(Lt) * es);
+  void* vit = Li ? bp.take<uint8_t>((size_t)B * H * d * vt_ld(Li) * es) : nullptr;
+  const int D = H * d;
+  for (int seg = 0; seg < (Li ? 2 : 1); ++seg) {
+    const int Lk = seg ? Li : Lt;
+    void* vtr = seg ? vit : vtt;
+    WAN_TRY(launch_transpose_v(c, seg ? vi : vt, vtr, vt_ld(Lk), B, Lk, H, d, f32));
+    AttnArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = q; a.ldq = D; a.q_row_len = D;
+    a.k = seg ? ki : kt; a.ldk = D; a.k_row_len = D;
+    a.vt = vtr; a.ld_vt = vt_ld(Lk);
+    a.o = o; a.ldo = D;
+    a.B = B; a.Lq = L; a.Lkv = Lk; a.H = H; a.head_dim = d;
+    a.accumulate = seg;
+    a.tag = "attn_cross";
+    WAN_TRY(attend(c, f32, a));
+  }
+  return WAN_OK;
+}
+
+int wan_ffn(const void* y, const void* w1, const void* b1, const void* w2, const void* b2, const float* gate,
+            float* x_inout, void* h_ws, int B, int L, int D, int F, int dtype, wan_stream_t stream) {
+  WAN_TRY(check_dtype(dtype));
+  const int f32 = dtype == WAN_F32;
+  if (!y || !w1 || !w2 || !x_inout || !h_ws || B <= 0 || L <= 0 || D <= 0 || F <= 0) return WAN_ERR_INVALID_ARG;
+  if (D % 32 || F % 32 || !aligned16(y) || !aligned16(w1) || !aligned16(w2) || !aligned16(x_inout) ||
+      !aligned16(h_ws) || (gate && !aligned16(gate)))
+    return WAN_ERR_UNSUPPORTED;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  const int M = B * L;
+  EpiParams e1 = epi_base(EPI_GELU, M, F, L, b1, f32);
+  e1.out = h_ws;
+  e1.ldo = F;
+  e1.out_f32 = f32;
+  WAN_TRY(proj(c, f32, y, D, D, w1, D, D, M, F, D, 0, e1, "gemm_ffn1_gelu"));
+  EpiParams e2 = epi_base(EPI_RESID, M, D, L, b2, f32);
+  e2.resid = x_inout;
+  e2.ldr = D;
+  e2.gate = gate;
+  e2.ld_gate = D;
+  return proj(c, f32, h_ws, F, F, w2, F, F, M, D, F, 0, e2, "gemm_ffn2_gate");
+}
+
+int wan_linear(const void* x, const void* w, const void* b, void* out, int M, int N, int K, int epilogue,
+               const float* gate, int rows_per_gate, int dtype, int out_dtype, wan_stream_t stream) {
+  WAN_TRY(check_dtype(dtype));
+  WAN_TRY(check_dtype(out_dtype));
+  const int f32 = dtype == WAN_F32;
+  if (!x || !w || !out || M <= 0 || N <= 0 || K <= 0) return WAN_ERR_INVALID_ARG;
+  if (epilogue != WAN_EPI_STORE && epilogue != WAN_EPI_GELU && epilogue != WAN_EPI_RESIDUAL) return WAN_ERR_INVALID_ARG;
+  if (gate && rows_per_gate <= 0) return WAN_ERR_INVALID_ARG;
+  if (f32 && out_dtype != WAN_F32) return WAN_ERR_UNSUPPORTED;
+  if (N % 32 || K % 8 || !aligned16(x) || !aligned16(w) || !aligned16(out) || (gate && !aligned16(gate)))
+    return WAN_ERR_UNSUPPORTED;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  const int kind = epilogue == WAN_EPI_STORE ? EPI_STORE : (epilogue == WAN_EPI_GELU ? EPI_GELU : EPI_RESID);
+  EpiParams ep = epi_base(kind, M, N, gate ? rows_per_gate : M, b, f32);
+  if (kind == EPI_RESID) {
+    ep.resid = static_cast<float*>(out);
+    ep.ldr = N;
+    ep.gate = gate;
+    ep.ld_gate = N;
+  } else {
+    ep.out = out;
+    ep.ldo = N;
+    ep.out_f32 = out_dtype == WAN_F32;
+  }
+  return proj(c, f32, x, K, K, w, K, K, M, N, K, 0, ep, "gemm_linear");
+}
+
+size_t wan_text_embed_workspace_size(int B, int Lt, int D, int dtype) {
+  if (B <= 0 || Lt <= 0 || D <= 0) return 0;
+  return (size_t)round_up((long long)B * Lt * D * (dtype == WAN_F32 ? 4 : 2), 1024);
+}
+
+int wan_text_embed(const void* text, const void* w1, const void* b1, const void* w2, const void* b2, void* ctx, int B,
+                   int Lt, int Ct, int D, int dtype, void* ws, size_t ws_bytes, wan_stream_t stream) {
+  WAN_TRY(check_dtype(dtype));
+  const int f32 = dtype == WAN_F32;
+  if (!text || !w1 || !w2 || !ctx || B <= 0 || Lt <= 0 || Ct <= 0 || D <= 0) return WAN_ERR_INVALID_ARG;
+  if (D % 32 || Ct % 8 || !aligned16(text) || !aligned16(w1) || !aligned16(w2) || !aligned16(ctx))
+    return WAN_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < wan_text_embed_workspace_size(B, Lt, D, dtype) || !aligned16(ws)) return WAN_ERR_WORKSPACE;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  const int M = B * Lt;
+  EpiParams e1 = epi_base(EPI_GELU, M, D, Lt, b1, f32);
+  e1.out = ws;
+  e1.ldo = D;
+  e1.out_f32 = f32;
+  WAN_TRY(proj(c, f32, text, Ct, Ct, w1, Ct, Ct, M, D, Ct, 0, e1, "gemm_text1_gelu"));
+  EpiParams e2 = epi_base(EPI_STORE, M, D, Lt, b2, f32);
+  e2.out = ctx;
+  e2.ldo = D;
+  e2.out_f32 = f32;
+  return proj(c, f32, ws, D, D, w2, D, D, M, D, D, 0, e2, "gemm_text2");
+}
+
+int wan_cfg_euler_step(float* x, const void* v_cond, const void* v_uncond, long long n, float guide_scale, float dt,
+                       int v_dtype, wan_stream_t stream) {
+  WAN_TRY(check_dtype(v_dtype));
+  if (n < 0) return WAN_ERR_INVALID_ARG;
+  if (n == 0) return WAN_OK;
+  if (!x || !v_cond || !v_uncond) return WAN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(v_cond) || !aligned16(v_uncond)) return WAN_ERR_UNSUPPORTED;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  return launch_cfg_euler(c, x, v_cond, v_uncond, n, guide_scale, dt, nullptr, v_dtype == WAN_F32);
+}
+
+size_t wan_dit_workspace_size(const wan_dit_config* cfg) {
+  if (validate_cfg(cfg) != WAN_OK) return 0;
+  return plan_forward(cfg, nullptr).bytes;
+}
+
+int wan_dit_forward(const wan_dit_config* cfg, const wan_dit_weights* w, const float* latent, int latent_broadcast,
+                    const float* t, const void* ctx_txt, const void* ctx_img, float* v_out, void* ws, size_t ws_bytes,
+                    wan_stream_t stream) {
+  if (!cfg) return WAN_ERR_INVALID_ARG;
+  const long long bstride = latent_broadcast ? 0 : (long long)cfg->c_in * cfg->frames * cfg->height * cfg->width;
+  return dit_forward_impl(cfg, w, latent, bstride, t, 1, ctx_txt, ctx_img, v_out, ws, ws_bytes, stream);
+}
+
+int wan_dit_guided_step(const wan_dit_config* cfg, const wan_dit_weights* w, float* x, const float* t_pair,
+                        float guide_scale, const void* ctx_txt, const void* ctx_img, float* v_ws, void* ws,
+                        size_t ws_bytes, wan_stream_t stream) {
+  if (!cfg || !x || !t_pair || !v_ws) return WAN_ERR_INVALID_ARG;
+  if (cfg->batch != 2) return WAN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(v_ws)) return WAN_ERR_UNSUPPORTED;
+  WAN_TRY(dit_forward_impl(cfg, w, x, 0, t_pair, 0, ctx_txt, ctx_img, v_ws, ws, ws_bytes, stream));
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  const long long n = (long long)cfg->c_out * cfg->frames * cfg->height * cfg->width;
+  return launch_cfg_euler(c, x, v_ws, v_ws + n, n, guide_scale, 0.f, t_pair, 1);
+}
+
+int wan_sample(const wan_dit_config* cfg, const wan_dit_weights* w, float* x, int steps, float guide_scale,
+               const void* ctx_txt, const void* ctx_img, float* t_sched, float* v_ws, void* ws, size_t ws_bytes,
+               wan_stream_t stream) {
+  if (!cfg || !x || !t_sched || steps <= 0) return WAN_ERR_INVALID_ARG;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  WAN_TRY(launch_schedule(c, t_sched, steps));
+  for (int k = 0; k < steps; ++k)
+    WAN_TRY(wan_dit_guided_step(cfg, w, x, t_sched + k, guide_scale, ctx_txt, ctx_img, v_ws, ws, ws_bytes, stream));
+  return WAN_OK;
+}
+
+int wan_profile_begin(int capacity) {
+  if (capacity <= 0) return WAN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  while (g_pool.size() < 2 * (size_t)capacity) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return WAN_ERR_CUDA;
+    g_pool.push_back(e);
+  }
+  g_recs.clear();
+  g_cap = (size_t)capacity;
+  g_prof_open = false;
+  g_prof_on = true;
+  return WAN_OK;
+}
+
+int wan_profile_end(const char** names, double* ms, int* counts, int max_kinds) {
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_on = false;
+    recs.swap(g_recs);
+  }
+  int nk = 0;
+  for (const ProfRec& r : recs) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return WAN_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return WAN_ERR_CUDA;
+    int k = 0;
+    while (k < nk && strcmp(names[k], r.kind) != 0) ++k;
+    if (k == nk) {
+      if (nk == max_kinds) continue;
+      names[nk] = r.kind;
+      ms[nk] = 0.0;
+      counts[nk] = 0;
+      ++nk;
+    }
+    ms[k] += t;
+    counts[k] += 1;
+  }
+  return nk;
+}
+
+}  // extern "C"

@@ -1,0 +1,352 @@
+// Flash-style attention on the 5th-generation tensor cores for the DiT's full
+// bidirectional self-attention and its short-context cross-attention:
+//   o = softmax(q k^T / sqrt(d)) v  per (batch, head), no mask.
+//
+// One CTA owns two 128-row query tiles of one (batch, head) and streams the whole key
+// sequence in 128-key tiles.  Tensor memory holds, per query tile, the score tile S
+// (128 fp32 columns; the bf16 probabilities P overwrite its first 64 columns) and the
+// output accumulator O (d fp32 columns): 2 x 256 = 512 columns.
+//   warp 0      TMA: Q once, then K and V^T tiles into 2-deep rings
+//   warp 1      tcgen05.mma from one thread: S_i = Q_i K^T (both operands in smem),
+//               O_i += P_i V (P from TMEM, V^T tile from smem), ping-ponging the tiles
+//   warps 2..9  softmax, one warpgroup per query tile, one thread per query row: fp32
+//               running max and sum, exp2 on the MUFU unit, lazy rescale of O in TMEM
+//               only when the running max grows by more than 2^8, final 1/l and store.
+// V arrives transposed ([d, keys], keys contiguous) so every MMA operand is K-major.
+// Ragged tails: keys past Lkv are zero-filled by TMA and masked to -inf; query rows
+// past Lq are computed on zero rows and not stored.
+#include "kernels.h"
+#include "wan_common.cuh"
+
+namespace wan {
+
+template <int HD>
+struct AttnCfg {
+  static constexpr int BQ = 128;
+  static constexpr int BKV = 128;
+  static constexpr int Q_BYTES = BQ * HD * 2;    // HD/64 boxes of 128 rows x 128 B
+  static constexpr int K_BYTES = BKV * HD * 2;   // HD/64 boxes of 128 rows x 128 B
+  static constexpr int V_BYTES = HD * BKV * 2;   // 2 boxes of HD rows x 128 B (64 keys)
+  static constexpr int Q_BOX = BQ * 128;         // bytes per 64-column box of a Q/K tile
+  static constexpr int V_BOX = HD * 128;         // bytes per 64-key box of a V^T tile
+  static constexpr int SMEM_TILES = 2 * Q_BYTES + 2 * K_BYTES + 2 * V_BYTES;
+  static constexpr int SMEM = SMEM_TILES + 256 + 1024;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int THREADS = 320;
+};
+
+struct AttnParams {
+  int Lq, Lkv, H;
+  int q_col, k_col;       // column offset of head 0 inside the q / k rows
+  int nq_pairs;           // ceil(ceil(Lq/128)/2)
+  float scale_log2;       // log2(e) / sqrt(d)
+  bf16* o;                // [B, Lq, ldo]
+  long long ldo;
+  int o_col;
+  int accumulate;         // o += result (decoupled cross-attention)
+};
+
+template <int HD>
+__global__ void __launch_bounds__(320, 1)
+    attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const AttnParams p, int* status) {
+  using Cfg = AttnCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                                  // [2][Q_BYTES]
+  uint8_t* sK = sQ + 2 * Cfg::Q_BYTES;                 // [2][K_BYTES]
+  uint8_t* sV = sK + 2 * Cfg::K_BYTES;                 // [2][V_BYTES]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::SMEM_TILES);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;   // [2]
+  uint64_t* k_empty = bars + 3;  // [2]
+  uint64_t* v_full = bars + 5;   // [2]
+  uint64_t* v_empty = bars + 7;  // [2]
+  uint64_t* s_full = bars + 9;   // [2] per query tile
+  uint64_t* p_ready = bars + 11; // [2] per query tile
+  uint64_t* drain = bars + 13;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 14);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x / p.nq_pairs;
+  const int qp = blockIdx.x - bh * p.nq_pairs;
+  const int b = bh / p.H;
+  const int h = bh - b * p.H;
+  const int q0 = qp * 256;
+  const int ntile = (q0 + 128 < p.Lq) ? 2 : 1;
+  const int nkv = (p.Lkv + Cfg::BKV - 1) / Cfg::BKV;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_ready[s], 128);
+    }
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    mbar_arrive_expect_tx(q_full, ntile * Cfg::Q_BYTES);
+    for (int i = 0; i < ntile; ++i)
+      for (int c = 0; c < HD / 64; ++c)
+        tma_load_3d(sQ + i * Cfg::Q_BYTES + c * Cfg::Q_BOX, &tmQ, q_full, p.q_col + h * HD + c * 64,
+                    q0 + i * 128, b);
+    uint32_t kissued = 0, vissued = 0;
+    bool ok = true;
+    for (int j = 0; j < nkv && ok; ++j) {
+      const int s = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!mbar_wait(&k_empty[s], ph ^ 1, status, kDevTimeoutAttn)) { ok = false; break; }
+      mbar_arrive_expect_tx(&k_full[s], Cfg::K_BYTES);
+      for (int c = 0; c < HD / 64; ++c)
+        tma_load_3d(sK + s * Cfg::K_BYTES + c * Cfg::Q_BOX, &tmK, &k_full[s], p.k_col + h * HD + c * 64,
+                    j * Cfg::BKV, b);
+      kissued = j + 1;
+      if (!mbar_wait(&v_empty[s], ph ^ 1, status, kDevTimeoutAttn)) { ok = false; break; }
+      mbar_arrive_expect_tx(&v_full[s], Cfg::V_BYTES);
+      for (int c = 0; c < 2; ++c)
+        tma_load_2d(sV + s * Cfg::V_BYTES + c * Cfg::V_BOX, &tmV, &v_full[s], j * Cfg::BKV + c * 64, bh * HD);
+      vissued = j + 1;
+    }
+    if (!ok) {  // error path: let issued copies land
+      const unsigned long long t0 = globaltimer_ns();
+      for (uint32_t j = (kissued > 2 ? kissued - 2 : 0); j < kissued; ++j)
+        while (!mbar_test(&k_full[j & 1], (j >> 1) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+      for (uint32_t j = (vissued > 2 ? vissued - 2 : 0); j < vissued; ++j)
+        while (!mbar_test(&v_full[j & 1], (j >> 1) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+      while (!mbar_test(q_full, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    constexpr uint32_t idS = make_idesc_bf16(128, Cfg::BKV);
+    constexpr uint32_t idO = make_idesc_bf16(128, HD);
+    bool ok = mbar_wait(q_full, 0, status, kDevTimeoutAttn) && mbar_wait(&k_full[0], 0, status, kDevTimeoutAttn);
+    auto issue_S = [&](int i, int ks) {
+      const uint32_t qa = smem_u32(sQ + i * Cfg::Q_BYTES);
+      const uint32_t ka = smem_u32(sK + ks * Cfg::K_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * Cfg::Q_BOX + (kk & 3) * 32;
+        tc_mma_ss(tmem_base + i * 256, make_sdesc_sw128(qa + off), make_sdesc_sw128(ka + off), idS,
+                  kk > 0 ? 1u : 0u);
+      }
+    };
+    auto issue_PV = [&](int i, int vs, uint32_t acc) {
+      const uint32_t va = smem_u32(sV + vs * Cfg::V_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < Cfg::BKV / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * Cfg::V_BOX + (kk & 3) * 32;
+        tc_mma_ts(tmem_base + i * 256 + 128, tmem_base + i * 256 + kk * 8, make_sdesc_sw128(va + off), idO,
+                  (acc | (uint32_t)kk) != 0 ? 1u : 0u);
+      }
+    };
+    if (ok) {
+      tc_fence_after();
+      for (int i = 0; i < ntile; ++i) {
+        issue_S(i, 0);
+        tc_commit(&s_full[i]);
+      }
+      tc_commit(&k_empty[0]);
+    }
+    for (int j = 0; j < nkv && ok; ++j) {
+      const int vs = j & 1;
+      const int ks = (j + 1) & 1;
+      if (!mbar_wait(&v_full[vs], (j >> 1) & 1, status, kDevTimeoutAttn)) { ok = false; break; }
+      for (int i = 0; i < ntile; ++i) {
+        if (!mbar_wait(&p_ready[i], j & 1, status, kDevTimeoutAttn)) { ok = false; break; }
+        tc_fence_after();
+        issue_PV(i, vs, j > 0 ? 1u : 0u);
+        if (i == ntile - 1) tc_commit(&v_empty[vs]);
+        if (j + 1 < nkv) {
+          if (i == 0) {
+            if (!mbar_wait(&k_full[ks], ((j + 1) >> 1) & 1, status, kDevTimeoutAttn)) { ok = false; break; }
+            tc_fence_after();
+          }
+          issue_S(i, ks);
+          if (i == ntile - 1) tc_commit(&k_empty[ks]);
+        }
+        tc_commit(&s_full[i]);  // S_{i,j+1} ready, or (last j) O_i final
+      }
+    }
+    if (!ok) {
+      tc_commit(drain);
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_test(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+    }
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------------- softmax
+    const int i = (warp - 2) >> 2;   // query tile of this warpgroup
+    const int quad = warp & 3;       // TMEM lane quadrant of this warp
+    if (i < ntile) {
+      const uint32_t tS = tmem_base + ((uint32_t)(quad * 32) << 16) + i * 256;
+      const uint32_t tO = tS + 128;
+      const float sl2 = p.scale_log2;
+      float m_used = -INFINITY;  // running max of the scaled logits (log2 units)
+      float l_sum = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nkv; ++j) {
+        if (!mbar_wait_warp(&s_full[i], j & 1, status, kDevTimeoutAttn)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+        const int valid = p.Lkv - j * Cfg::BKV;  // >= 1
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float s = __uint_as_float(sr[c][e]);
+            if (c * 32 + e >= valid) s = -INFINITY;
+            sr[c][e] = __float_as_uint(s);
+            mt = fmaxf(mt, s);
+          }
+        mt *= sl2;
+        // Lazy rescale: a row moves its reference max only when the tile max exceeds it
+        // by more than 8 (a factor 256 in the exponentials).  The O update is done by the
+        // whole warp (tcgen05.ld/st are warp-collective), with alpha = 1 for rows that
+        // keep their max.
+        const bool need = mt > m_used + 8.0f;
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2_approx(m_used - mt) : 1.0f;
+          l_sum *= alpha;
+#pragma unroll 1
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t orr[32];
+            tmem_ld32(tO + c * 32, orr);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+            tmem_st32(tO + c * 32, orr);
+          }
+        }
+        if (need) m_used = mt;
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * e]), sl2, -m_used));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * e + 1]), sl2, -m_used));
+            pk[e] = pack_bf16x2(p0, p1);
+            const float2 q = unpack_bf16x2(pk[e]);
+            rs += q.x + q.y;
+          }
+          tmem_st16(tS + c * 16, pk);
+        }
+        l_sum += rs;
+        tc_fence_before();
+        mbar_arrive(&p_ready[i]);
+      }
+      if (ok && mbar_wait_warp(&s_full[i], nkv & 1, status, kDevTimeoutAttn)) {
+        tc_fence_after();
+        const float inv = 1.0f / l_sum;
+        const int qrow = q0 + i * 128 + quad * 32 + lane;
+        bf16* orow = p.o + ((long long)b * p.Lq + qrow) * p.ldo + p.o_col + h * HD;
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(tO + c * 32, orr);
+          if (qrow < p.Lq) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float v[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) v[u] = __uint_as_float(orr[e * 8 + u]) * inv;
+              if (p.accumulate) {
+                const uint4 prev = dst[e];
+                const uint32_t pw[4] = {prev.x, prev.y, prev.z, prev.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const float2 f = unpack_bf16x2(pw[u]);
+                  v[2 * u] += f.x;
+                  v[2 * u + 1] += f.y;
+                }
+              }
+              uint4 o4;
+              o4.x = pack_bf16x2(v[0], v[1]);
+              o4.y = pack_bf16x2(v[2], v[3]);
+              o4.z = pack_bf16x2(v[4], v[5]);
+              o4.w = pack_bf16x2(v[6], v[7]);
+              dst[e] = o4;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+}
+
+template <int HD>
+static int launch_attn(const LaunchCtx& c, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const AttnParams& p, int B, const char* tag) {
+  using Cfg = AttnCfg<HD>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(attn_bf16_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
+        cudaSuccess)
+      return WAN_ERR_CUDA;
+    attr_set = true;
+  }
+  const long long grid = (long long)B * p.H * p.nq_pairs;
+  count_launch(tag, c.stream, true);
+  attn_bf16_tc_kernel<HD><<<(unsigned)grid, Cfg::THREADS, Cfg::SMEM, c.stream>>>(tq, tk, tv, p, c.dev_status);
+  count_launch(tag, c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+int attention_bf16(const LaunchCtx& c, const AttnArgs& a) {
+  if (a.head_dim != 64 && a.head_dim != 128) return WAN_ERR_UNSUPPORTED;
+  if (a.Lq <= 0 || a.Lkv <= 0) return WAN_OK;
+  const int HD = a.head_dim;
+  CUtensorMap tq, tk, tv;
+  int st = make_tmap_3d(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.q_row_len, (uint64_t)a.Lq,
+                        (uint64_t)a.B, (uint64_t)a.ldq * 2, (uint64_t)a.ldq * 2 * a.Lq, 64, 128);
+  if (st != WAN_OK) return st;
+  st = make_tmap_3d(&tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.k_row_len, (uint64_t)a.Lkv,
+                    (uint64_t)a.B, (uint64_t)a.ldk * 2, (uint64_t)a.ldk * 2 * a.Lkv, 64, 128);
+  if (st != WAN_OK) return st;
+  st = make_tmap_2d(&tv, a.vt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.Lkv,
+                    (uint64_t)a.B * a.H * HD, (uint64_t)a.ld_vt * 2, 64, (uint32_t)HD);
+  if (st != WAN_OK) return st;
+  AttnParams p;
+  p.Lq = a.Lq;
+  p.Lkv = a.Lkv;
+  p.H = a.H;
+  p.q_col = a.q_col;
+  p.k_col = a.k_col;
+  p.nq_pairs = ((a.Lq + 127) / 128 + 1) / 2;
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
+  p.o = static_cast<bf16*>(a.o);
+  p.ldo = a.ldo;
+  p.o_col = a.o_col;
+  p.accumulate = a.accumulate;
+  const char* tag = a.tag ? a.tag : "attn";
+  return HD == 128 ? launch_attn<128>(c, tq, tk, tv, p, a.B, tag) : launch_attn<64>(c, tq, tk, tv, p, a.B, tag);
+}
+
+}  // namespace wan

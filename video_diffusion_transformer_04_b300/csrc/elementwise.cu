@@ -1,0 +1,421 @@
+// Bandwidth-bound passes of the DiT step: LayerNorm + AdaLN modulation, fused CFG +
+// Euler update, the patch gather feeding the patchify GEMM, and the small kernels of
+// the time embedding, RoPE table and layout changes.
+#include "kernels.h"
+
+namespace wan {
+
+// ------------------------------------------------------------------ LayerNorm + modulation
+// One 128-thread CTA per token row; the row stays in registers between the mean, the
+// (centred) variance and the normalisation.  y = (x - mu) * rstd * (1 + scale) + shift.
+template <int NV, typename OutT>
+__global__ void __launch_bounds__(128) ln_mod_kernel(const float* __restrict__ x, const float* __restrict__ shift,
+                                                     const float* __restrict__ scale, long long mod_bstride,
+                                                     OutT* __restrict__ y, int L, int D, float eps) {
+  __shared__ float red[4];
+  const int row = blockIdx.x;
+  const int b = row / L;
+  const int t = threadIdx.x;
+  const int nv4 = D >> 2;
+  const float4* xr = reinterpret_cast<const float4*>(x + (long long)row * D);
+  float4 v[NV];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = t + i * 128;
+    v[i] = c < nv4 ? xr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+    s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+  }
+  auto block_sum = [&](float a) {
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    __syncthreads();
+    if ((t & 31) == 0) red[t >> 5] = a;
+    __syncthreads();
+    return (red[0] + red[1]) + (red[2] + red[3]);
+  };
+  const float mean = block_sum(s) / (float)D;
+  float q = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = t + i * 128;
+    if (c < nv4) {
+      const float a0 = v[i].x - mean, a1 = v[i].y - mean, a2 = v[i].z - mean, a3 = v[i].w - mean;
+      q += (a0 * a0 + a1 * a1) + (a2 * a2 + a3 * a3);
+    }
+  }
+  const float var = block_sum(q) / (float)D;
+  const float rstd = rsqrtf(var + eps);
+  const float* sh = shift ? shift + (long long)b * mod_bstride : nullptr;
+  const float* sc = scale ? scale + (long long)b * mod_bstride : nullptr;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = t + i * 128;
+    if (c >= nv4) continue;
+    float o[4] = {(v[i].x - mean) * rstd, (v[i].y - mean) * rstd, (v[i].z - mean) * rstd, (v[i].w - mean) * rstd};
+    if (sc) {
+      const float4 s4 = reinterpret_cast<const float4*>(sc)[c];
+      o[0] *= 1.f + s4.x; o[1] *= 1.f + s4.y; o[2] *= 1.f + s4.z; o[3] *= 1.f + s4.w;
+    }
+    if (sh) {
+      const float4 h4 = reinterpret_cast<const float4*>(sh)[c];
+      o[0] += h4.x; o[1] += h4.y; o[2] += h4.z; o[3] += h4.w;
+    }
+    if constexpr (sizeof(OutT) == 4) {
+      reinterpret_cast<float4*>(y + (long long)row * D)[c] = make_float4(o[0], o[1], o[2], o[3]);
+    } else {
+      uint2 u;
+      u.x = pack_bf16x2(o[0], o[1]);
+      u.y = pack_bf16x2(o[2], o[3]);
+      reinterpret_cast<uint2*>(y + (long long)row * D)[c] = u;
+    }
+  }
+}
+
+template <typename OutT>
+static void ln_dispatch(const LaunchCtx& c, const float* x, const float* sh, const float* sc, long long bs, OutT* y,
+                        int rows, int L, int D, float eps) {
+  const int nv = (D / 4 + 127) / 128;
+  if (nv <= 1) ln_mod_kernel<1, OutT><<<rows, 128, 0, c.stream>>>(x, sh, sc, bs, y, L, D, eps);
+  else if (nv <= 3) ln_mod_kernel<3, OutT><<<rows, 128, 0, c.stream>>>(x, sh, sc, bs, y, L, D, eps);
+  else if (nv <= 10) ln_mod_kernel<10, OutT><<<rows, 128, 0, c.stream>>>(x, sh, sc, bs, y, L, D, eps);
+  else ln_mod_kernel<16, OutT><<<rows, 128, 0, c.stream>>>(x, sh, sc, bs, y, L, D, eps);
+}
+
+int launch_ln_mod(const LaunchCtx& c, const float* x, const float* shift, const float* scale, long long mod_bstride,
+                  void* y, int out_f32, int rows, int L, int D, float eps) {
+  if (rows <= 0) return WAN_OK;
+  if (D % 4 != 0 || D > 8192) return WAN_ERR_UNSUPPORTED;
+  count_launch("ln_modulate", c.stream, true);
+  if (out_f32) ln_dispatch<float>(c, x, shift, scale, mod_bstride, static_cast<float*>(y), rows, L, D, eps);
+  else ln_dispatch<bf16>(c, x, shift, scale, mod_bstride, static_cast<bf16*>(y), rows, L, D, eps);
+  count_launch("ln_modulate", c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ CFG + Euler
+// x <- x + dt * (vu + s * (vc - vu)), four elements per thread per iteration (16-byte
+// x accesses), grid-stride; a scalar loop takes the n % 4 tail.
+template <typename VT>
+__device__ __forceinline__ void load4(const VT* p, long long i, float* o);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, long long i, float* o) {
+  const float4 a = *reinterpret_cast<const float4*>(p + i);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+}
+template <>
+__device__ __forceinline__ void load4<bf16>(const bf16* p, long long i, float* o) {
+  const uint2 a = *reinterpret_cast<const uint2*>(p + i);
+  const float2 lo = unpack_bf16x2(a.x), hi = unpack_bf16x2(a.y);
+  o[0] = lo.x; o[1] = lo.y; o[2] = hi.x; o[3] = hi.y;
+}
+template <typename VT>
+__device__ __forceinline__ float load1(const VT* p, long long i) {
+  if constexpr (sizeof(VT) == 4) return p[i];
+  else return bf2f(p[i]);
+}
+
+template <typename VT>
+__global__ void __launch_bounds__(256) cfg_euler_kernel(float* __restrict__ x, const VT* __restrict__ vc,
+                                                        const VT* __restrict__ vu, long long n, float s, float dt,
+                                                        const float* __restrict__ t_pair) {
+  if (t_pair) dt = t_pair[1] - t_pair[0];
+  const long long n4 = n >> 2;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < n4; g += stride) {
+    const long long i = g << 2;
+    float a[4], c[4], u[4];
+    load4<float>(x, i, a);
+    load4<VT>(vc, i, c);
+    load4<VT>(vu, i, u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) a[k] = a[k] + dt * (u[k] + s * (c[k] - u[k]));
+    *reinterpret_cast<float4*>(x + i) = make_float4(a[0], a[1], a[2], a[3]);
+  }
+  if (blockIdx.x == 0)
+    for (long long i = (n4 << 2) + threadIdx.x; i < n; i += blockDim.x) {
+      const float c1 = load1<VT>(vc, i), u1 = load1<VT>(vu, i);
+      x[i] = x[i] + dt * (u1 + s * (c1 - u1));
+    }
+}
+
+int launch_cfg_euler(const LaunchCtx& c, float* x, const void* vc, const void* vu, long long n, float s, float dt,
+                     const float* t_pair, int v_f32) {
+  if (n <= 0) return WAN_OK;
+  long long blocks = ((n >> 2) + 255) / 256;
+  const long long cap = (long long)c.num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  count_launch("cfg_euler", c.stream, true);
+  if (v_f32)
+    cfg_euler_kernel<float><<<(unsigned)blocks, 256, 0, c.stream>>>(x, static_cast<const float*>(vc),
+                                                                   static_cast<const float*>(vu), n, s, dt, t_pair);
+  else
+    cfg_euler_kernel<bf16><<<(unsigned)blocks, 256, 0, c.stream>>>(x, static_cast<const bf16*>(vc),
+                                                                  static_cast<const bf16*>(vu), n, s, dt, t_pair);
+  count_launch("cfg_euler", c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ patch gather
+// A row of token m = (b, f, i, j) holds latent[b, c, f, 2i+di, 2j+dj] at column
+// c*4 + di*2 + dj.  bf16 output keeps the value exactly as a two-term split:
+// columns [0, kpad) hold hi = bf16(v), columns [kpad, 2 kpad) hold lo = bf16(v - hi),
+// padding columns are zero.  fp32 output has kpad = C*4 columns.
+__global__ void patch_gather_kernel(const float* __restrict__ lat, long long lat_bstride, void* __restrict__ A,
+                                    int out_f32, int B, int C, int F, int H, int W, int kpad) {
+  const int Hp = H >> 1, Wp = W >> 1;
+  const long long L = (long long)F * Hp * Wp;
+  const long long total = (long long)B * L * C;
+  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(g % C);
+    const long long m = g / C;
+    const int b = (int)(m / L);
+    const long long l = m - (long long)b * L;
+    const int f = (int)(l / ((long long)Hp * Wp));
+    const int i = (int)((l / Wp) % Hp);
+    const int j = (int)(l % Wp);
+    const float* src = lat + (long long)b * lat_bstride + (((long long)c * F + f) * H + 2 * i) * W + 2 * j;
+    const float v[4] = {src[0], src[1], src[W], src[W + 1]};
+    if (out_f32) {
+      float* row = static_cast<float*>(A) + m * kpad;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) row[c * 4 + k] = v[k];
+    } else {
+      bf16* row = static_cast<bf16*>(A) + m * (2LL * kpad);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const bf16 hi = __float2bfloat16_rn(v[k]);
+        row[c * 4 + k] = hi;
+        row[kpad + c * 4 + k] = __float2bfloat16_rn(v[k] - bf2f(hi));
+      }
+      if (c == 0)
+        for (int k = C * 4; k < kpad; ++k) {
+          row[k] = __float2bfloat16_rn(0.f);
+          row[kpad + k] = __float2bfloat16_rn(0.f);
+        }
+    }
+  }
+}
+
+int launch_patch_gather(const LaunchCtx& c, const float* latent, long long latent_bstride, void* A, int out_f32,
+                        int B, int C, int F, int H, int W, int kpad) {
+  const long long total = (long long)B * F * (H / 2) * (W / 2) * C;
+  if (total <= 0) return WAN_OK;
+  long long blocks = (total + 255) / 256;
+  if (blocks > (long long)c.num_sms * 16) blocks = (long long)c.num_sms * 16;
+  count_launch("patch_gather", c.stream, true);
+  patch_gather_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>(latent, latent_bstride, A, out_f32, B, C, F, H, W,
+                                                              kpad);
+  count_launch("patch_gather", c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ RoPE table
+// (cos, sin) of pos * theta^(-2j/d_a) for every axis a, grid position and pair j,
+// evaluated in double precision.
+__global__ void rope_table_kernel(float2* tab, RopeGeom g, float theta) {
+  const int total = g.Fg * g.nf + g.Hg * g.nh + g.Wg * g.nw;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+    int r = e, pairs, pos, j;
+    if (r < g.Fg * g.nf) { pairs = g.nf; pos = r / pairs; j = r % pairs; }
+    else if ((r -= g.Fg * g.nf) < g.Hg * g.nh) { pairs = g.nh; pos = r / pairs; j = r % pairs; }
+    else { r -= g.Hg * g.nh; pairs = g.nw; pos = r / pairs; j = r % pairs; }
+    const double ang = (double)pos * pow((double)theta, -2.0 * j / (2.0 * pairs));
+    tab[e] = make_float2((float)cos(ang), (float)sin(ang));
+  }
+}
+
+int launch_rope_table(const LaunchCtx& c, float2* tab, int Fg, int Hg, int Wg, int head_dim, float theta) {
+  RopeGeom g = rope_geom(tab, Fg, Hg, Wg, head_dim);
+  const int total = Fg * g.nf + Hg * g.nh + Wg * g.nw;
+  count_launch("rope_table", c.stream, true);
+  rope_table_kernel<<<(total + 255) / 256, 256, 0, c.stream>>>(tab, g, theta);
+  count_launch("rope_table", c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ time embedding
+// s[b] = [cos(tau w_k), sin(tau w_k)], tau = 1000 t[b], w_k = 10000^(-k/half), in double.
+__global__ void sinusoid_kernel(const float* t, int t_stride, float* s, int dim) {
+  const int b = blockIdx.x;
+  const int half = dim / 2;
+  const double tau = 1000.0 * (double)t[b * t_stride];
+  for (int k = threadIdx.x; k < half; k += blockDim.x) {
+    const double a = tau * pow(10000.0, -(double)k / half);
+    s[(long long)b * dim + k] = (float)cos(a);
+    s[(long long)b * dim + half + k] = (float)sin(a);
+  }
+}
+
+int launch_sinusoid(const LaunchCtx& c, const float* t, int t_stride, float* s, int B, int dim) {
+  count_launch("sinusoid", c.stream, true);
+  sinusoid_kernel<<<B, 128, 0, c.stream>>>(t, t_stride, s, dim);
+  count_launch("sinusoid", c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+
+// One warp per output feature n; lanes stride over K.
+__global__ void __launch_bounds__(256) small_linear_kernel(const float* __restrict__ x, const void* __restrict__ W,
+                                                           const void* __restrict__ bias, int w_f32,
+                                                           float* __restrict__ out, int B, int N, int K,
+                                                           int act_in, int act_out) {
+  const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (n >= N) return;
+  for (int b = 0; b < B; ++b) {
+    float acc = 0.f;
+    for (int k = lane; k < K; k += 32) {
+      float xv = x[(long long)b * K + k];
+      if (act_in) xv = silu_f(xv);
+      const float wv = w_f32 ? static_cast<const float*>(W)[(long long)n * K + k]
+                             : bf2f(static_cast<const bf16*>(W)[(long long)n * K + k]);
+      acc = fmaf(wv, xv, acc);
+    }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      if (bias) acc += w_f32 ? static_cast<const float*>(bias)[n] : bf2f(static_cast<const bf16*>(bias)[n]);
+      if (act_out) acc = silu_f(acc);
+      out[(long long)b * N + n] = acc;
+    }
+  }
+}
+
+int launch_small_linear(const LaunchCtx& c, const float* x, const void* W, const void* bias, int w_f32, float* out,
+                        int B, int N, int K, int act_in, int act_out) {
+  count_launch("time_mlp", c.stream, true);
+  small_linear_kernel<<<(N + 7) / 8, 256, 0, c.stream>>>(x, W, bias, w_f32, out, B, N, K, act_in, act_out);
+  count_launch("time_mlp", c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+struct ModPtrs {
+  const void* p[64];
+};
+
+__global__ void block_mods_kernel(const float* __restrict__ e0, ModPtrs mp, int nblk, int w_f32,
+                                  float* __restrict__ mods, int B, int D) {
+  const long long per = (long long)B * 6 * D;
+  const long long total = per * nblk;
+  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (long long)gridDim.x * blockDim.x) {
+    const int blk = (int)(g / per);
+    const long long r = g - blk * per;
+    const int b = (int)(r / (6LL * D));
+    const int kn = (int)(r - (long long)b * 6 * D);
+    const float m = w_f32 ? static_cast<const float*>(mp.p[blk])[kn] : bf2f(static_cast<const bf16*>(mp.p[blk])[kn]);
+    mods[g] = e0[(long long)b * 6 * D + kn] + m;
+  }
+}
+
+int launch_block_mods(const LaunchCtx& c, const float* e0, const void* const* mod_ptrs, int nblk, int w_f32,
+                      float* mods, int B, int D) {
+  for (int s = 0; s < nblk; s += 64) {
+    ModPtrs mp;
+    const int n = nblk - s < 64 ? nblk - s : 64;
+    for (int i = 0; i < n; ++i) mp.p[i] = mod_ptrs[s + i];
+    const long long total = (long long)n * B * 6 * D;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    count_launch("block_mods", c.stream, true);
+    block_mods_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>(e0, mp, n, w_f32, mods + (long long)s * B * 6 * D, B, D);
+    count_launch("block_mods", c.stream, false);
+    if (cudaGetLastError() != cudaSuccess) return WAN_ERR_CUDA;
+  }
+  return WAN_OK;
+}
+
+// ------------------------------------------------------------------ layout helpers
+template <typename T>
+__global__ void transpose_v_kernel(const T* __restrict__ v, T* __restrict__ vt, long long ld_vt, int L, int H, int d) {
+  __shared__ T tile[32][33];
+  const int bh = blockIdx.z;
+  const int b = bh / H, h = bh - (bh / H) * H;
+  const int l0 = blockIdx.x * 32, d0 = blockIdx.y * 32;
+  const long long D = (long long)H * d;
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int l = l0 + r, dd = d0 + threadIdx.x;
+    if (l < L && dd < d) tile[r][threadIdx.x] = v[((long long)b * L + l) * D + h * d + dd];
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int dd = d0 + r, l = l0 + threadIdx.x;
+    if (l < L && dd < d) vt[((long long)bh * d + dd) * ld_vt + l] = tile[threadIdx.x][r];
+  }
+}
+
+int launch_transpose_v(const LaunchCtx& c, const void* v, void* vt, long long ld_vt, int B, int L, int H, int d,
+                       int f32) {
+  if (B * L <= 0) return WAN_OK;
+  dim3 grid((L + 31) / 32, (d + 31) / 32, B * H), block(32, 8);
+  count_launch("transpose_v", c.stream, true);
+  if (f32)
+    transpose_v_kernel<float><<<grid, block, 0, c.stream>>>(static_cast<const float*>(v), static_cast<float*>(vt),
+                                                            ld_vt, L, H, d);
+  else
+    transpose_v_kernel<bf16><<<grid, block, 0, c.stream>>>(static_cast<const bf16*>(v), static_cast<bf16*>(vt), ld_vt,
+                                                           L, H, d);
+  count_launch("transpose_v", c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+template <typename T>
+__global__ void rope_apply_kernel(const T* __restrict__ in, T* __restrict__ out, RopeGeom g, long long rows, int L,
+                                  int H, int d) {
+  const long long pairs_per_row = (long long)H * d / 2;
+  const long long total = rows * pairs_per_row;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
+    const long long m = e / pairs_per_row;
+    const int pr = (int)(e - m * pairs_per_row);
+    const int l = (int)(m % L);
+    const int dd0 = (pr * 2) % d;
+    float v[2];
+    if constexpr (sizeof(T) == 4) {
+      v[0] = in[m * H * d + 2 * pr];
+      v[1] = in[m * H * d + 2 * pr + 1];
+    } else {
+      v[0] = bf2f(in[m * H * d + 2 * pr]);
+      v[1] = bf2f(in[m * H * d + 2 * pr + 1]);
+    }
+    epi_rope<2>(g, d, dd0, l, v);
+    if constexpr (sizeof(T) == 4) {
+      out[m * H * d + 2 * pr] = v[0];
+      out[m * H * d + 2 * pr + 1] = v[1];
+    } else {
+      out[m * H * d + 2 * pr] = __float2bfloat16_rn(v[0]);
+      out[m * H * d + 2 * pr + 1] = __float2bfloat16_rn(v[1]);
+    }
+  }
+}
+
+int launch_rope_apply(const LaunchCtx& c, const void* in, void* out, const RopeGeom& g, int B, int L, int H, int d,
+                      int f32) {
+  const long long total = (long long)B * L * H * d / 2;
+  if (total <= 0) return WAN_OK;
+  long long blocks = (total + 255) / 256;
+  if (blocks > (long long)c.num_sms * 16) blocks = (long long)c.num_sms * 16;
+  count_launch("rope_apply", c.stream, true);
+  if (f32)
+    rope_apply_kernel<float><<<(unsigned)blocks, 256, 0, c.stream>>>(static_cast<const float*>(in),
+                                                                     static_cast<float*>(out), g, (long long)B * L, L,
+                                                                     H, d);
+  else
+    rope_apply_kernel<bf16><<<(unsigned)blocks, 256, 0, c.stream>>>(static_cast<const bf16*>(in),
+                                                                    static_cast<bf16*>(out), g, (long long)B * L, L, H,
+                                                                    d);
+  count_launch("rope_apply", c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+__global__ void schedule_kernel(float* ts, int steps) {
+  for (int k = threadIdx.x; k <= steps; k += blockDim.x) ts[k] = 1.0f - (float)k / (float)steps;
+}
+
+int launch_schedule(const LaunchCtx& c, float* ts, int steps) {
+  count_launch("schedule", c.stream, true);
+  schedule_kernel<<<1, 256, 0, c.stream>>>(ts, steps);
+  count_launch("schedule", c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+}  // namespace wan

@@ -1,0 +1,213 @@
+// bf16 GEMM on the 5th-generation tensor cores: C[M, N] = A[M, K] * B[N, K]^T with a
+// fused epilogue (epilogue.cuh).  Every projection of the DiT block (QKV, output,
+// cross-attention, FFN, patchify, head, text projection) runs through this kernel.
+//
+// Design (one CTA per SM, persistent over output tiles of 128 x BN):
+//   warp 0      TMA producer: A and B tiles (128-byte swizzle) into a STAGES-deep ring
+//   warp 1      allocates TMEM, issues tcgen05.mma (M=128, N=BN, K=16) from one thread,
+//               commits each consumed stage back to the producer
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane = one output
+//               row per thread), bias/GELU/RoPE/gated residual/layout, global stores
+// The accumulator is double-buffered in TMEM (2 x BN columns), so the epilogue of tile
+// i overlaps the main loop of tile i+1.
+#include <cstdio>
+
+#include "epilogue.cuh"
+#include "kernels.h"
+
+namespace wan {
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int BM = 128;
+  static constexpr int BK = 64;  // one 128-byte swizzle row of bf16
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
+};
+
+template <int BN>
+__global__ void __launch_bounds__(192, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const EpiParams ep, int M, int N, int K, int kb_period, int* status) {
+  using Cfg = GemmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
+  uint64_t* empty = full + Cfg::STAGES;
+  uint64_t* tfull = empty + Cfg::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_m = (M + Cfg::BM - 1) / Cfg::BM;
+  const int num_n = (N + BN - 1) / BN;
+  const int num_k = (K + Cfg::BK - 1) / Cfg::BK;
+  const int num_tiles = num_m * num_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, issued_phase = 0;  // bit s: stage s holds a load; its phase
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      const int mb = tile / num_n, nb = tile - (tile / num_n) * num_n;
+      for (int kb = 0; kb < num_k; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, status, kDevTimeoutGemm)) { ok = false; break; }
+        uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+        const int kb_b = kb_period ? (kb % kb_period) : kb;
+        tma_load_2d(sa, &tmA, &full[stage], kb * Cfg::BK, mb * Cfg::BM);
+        tma_load_2d(sa + Cfg::A_BYTES, &tmB, &full[stage], kb_b * Cfg::BK, nb * BN);
+        issued |= 1u << stage;
+        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+    if (!ok) {  // error path: let the copies in flight land before the CTA exits
+      for (int s = 0; s < Cfg::STAGES; ++s)
+        if (issued & (1u << s)) {
+          const unsigned long long t0 = globaltimer_ns();
+          while (!mbar_test(&full[s], (issued_phase >> s) & 1u) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+        }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc = make_idesc_bf16(Cfg::BM, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      if (!mbar_wait(&tempty[acc], acc_phase ^ 1, status, kDevTimeoutGemm)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < num_k; ++kb) {
+        if (!mbar_wait(&full[stage], phase, status, kDevTimeoutGemm)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+        const uint64_t adesc = make_sdesc_sw128(sa);
+        const uint64_t bdesc = make_sdesc_sw128(sa + Cfg::A_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < Cfg::BK / 16; ++kk)
+          tc_mma_ss(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                    (kb | kk) != 0 ? 1u : 0u);
+        tc_commit(&empty[stage]);
+        if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+      tc_commit(&tfull[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+    if (!ok) {  // error path: wait for the MMAs in flight before TMEM is released
+      tc_commit(drain);
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_test(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+    }
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------------- epilogue
+    const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad + 32) belong to this warp
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int mb = tile / num_n, nb = tile - (tile / num_n) * num_n;
+      if (!mbar_wait_warp(&tfull[acc], acc_phase, status, kDevTimeoutGemm)) break;
+      tc_fence_after();
+      const int row = mb * Cfg::BM + quad * 32 + lane;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c * 32, r);
+        const int n0 = nb * BN + c * 32;
+        if (row < M && n0 < N) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          epilogue_chunk<32>(ep, row, n0, v);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+}
+
+template <int BN>
+static int launch_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb, const EpiParams& ep,
+                       int M, int N, int K, int kb_period, const char* tag) {
+  using Cfg = GemmCfg<BN>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
+        cudaSuccess)
+      return WAN_ERR_CUDA;
+    attr_set = true;
+  }
+  const int tiles = ((M + 127) / 128) * ((N + BN - 1) / BN);
+  const int grid = tiles < c.num_sms ? tiles : c.num_sms;
+  count_launch(tag, c.stream, true);
+  gemm_bf16_tc_kernel<BN><<<grid, 192, Cfg::SMEM, c.stream>>>(ta, tb, ep, M, N, K, kb_period, c.dev_status);
+  count_launch(tag, c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+int gemm_bf16(const LaunchCtx& c, const bf16* A, long long lda, int a_cols, const bf16* B, long long ldb, int b_cols,
+              int M, int N, int K, int kb_period, const EpiParams& ep, const char* tag) {
+  if (M <= 0 || N <= 0 || K <= 0) return WAN_OK;
+  int bn = (N % 256 == 0) ? 256 : (N % 128 == 0 ? 128 : 64);
+  CUtensorMap ta, tb;
+  int st = make_tmap_2d(&ta, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a_cols, (uint64_t)M,
+                        (uint64_t)lda * 2, 64, 128);
+  if (st != WAN_OK) return st;
+  st = make_tmap_2d(&tb, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)b_cols, (uint64_t)N, (uint64_t)ldb * 2,
+                    64, (uint32_t)bn);
+  if (st != WAN_OK) return st;
+  switch (bn) {
+    case 256: return launch_gemm<256>(c, ta, tb, ep, M, N, K, kb_period, tag);
+    case 128: return launch_gemm<128>(c, ta, tb, ep, M, N, K, kb_period, tag);
+    default: return launch_gemm<64>(c, ta, tb, ep, M, N, K, kb_period, tag);
+  }
+}
+
+}  // namespace wan

@@ -1,0 +1,92 @@
+// Internal interface between the kernel files and the C-ABI layer (api.cu).
+#pragma once
+
+#include "epilogue.cuh"
+#include "wan_common.cuh"
+
+namespace wan {
+
+// ------------------------------------------------------------------ tensor maps (api.cu)
+// 2D / 3D tiled maps with 128-byte swizzle and zero fill outside the tensor.
+int make_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t d0,
+                 uint64_t d1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1);
+int make_tmap_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t d0,
+                 uint64_t d1, uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,
+                 uint32_t box1);
+
+// ------------------------------------------------------------------ GEMMs
+// bf16 tcgen05 GEMM: C = A[M, K] * B[N, K]^T -> epilogue.  a_cols / b_cols: valid
+// columns of A / B (TMA zero-fills beyond); lda / ldb: row strides in elements.
+// kb_period > 0: the B k-block index wraps modulo kb_period (A = [hi | lo] split).
+int gemm_bf16(const LaunchCtx& c, const bf16* A, long long lda, int a_cols, const bf16* B, long long ldb,
+              int b_cols, int M, int N, int K, int kb_period, const EpiParams& ep, const char* tag);
+// fp32 SIMT GEMM (parity path): same contract, fp32 operands.
+int gemm_f32(const LaunchCtx& c, const float* A, long long lda, const float* B, long long ldb, int M, int N, int K,
+             const EpiParams& ep, const char* tag);
+
+// ------------------------------------------------------------------ attention
+struct AttnArgs {
+  const void* q;
+  long long ldq;   // row stride of q (elements)
+  int q_row_len;   // valid elements per q row
+  int q_col;       // column of head 0
+  const void* k;
+  long long ldk;
+  int k_row_len;
+  int k_col;
+  const void* vt;  // V transposed: row (b*H + h)*d + dd, column = key
+  long long ld_vt;
+  void* o;
+  long long ldo;
+  int o_col;
+  int B, Lq, Lkv, H, head_dim;
+  int accumulate;  // o += result
+  const char* tag; // profiler label of the launch
+};
+int attention_bf16(const LaunchCtx& c, const AttnArgs& a);
+int attention_f32(const LaunchCtx& c, const AttnArgs& a);
+
+// ------------------------------------------------------------------ elementwise / small kernels
+int launch_ln_mod(const LaunchCtx& c, const float* x, const float* shift, const float* scale, long long mod_bstride,
+                  void* y, int out_f32, int rows, int L, int D, float eps);
+int launch_cfg_euler(const LaunchCtx& c, float* x, const void* vc, const void* vu, long long n, float s, float dt,
+                     const float* t_pair, int v_f32);
+int launch_patch_gather(const LaunchCtx& c, const float* latent, long long latent_bstride, void* A, int out_f32,
+                        int B, int C, int F, int H, int W, int kpad);
+int launch_rope_table(const LaunchCtx& c, float2* tab, int Fg, int Hg, int Wg, int head_dim, float theta);
+// t[b * t_stride] (t_stride 0: one timestep shared by the batch).
+int launch_sinusoid(const LaunchCtx& c, const float* t, int t_stride, float* s, int B, int dim);
+// out[b, n] = act_out(sum_k W[n, k] * act_in(x[b, k]) + bias[n]); act: 0 none, 1 SiLU.
+int launch_small_linear(const LaunchCtx& c, const float* x, const void* W, const void* bias, int w_f32, float* out,
+                        int B, int N, int K, int act_in, int act_out);
+// mods[blk][b][k][n] = e0[b][k*D + n] + mod_blk[k][n] for `nblk` blocks.
+int launch_block_mods(const LaunchCtx& c, const float* e0, const void* const* mod_ptrs, int nblk, int w_f32,
+                      float* mods, int B, int D);
+// v [B, L, H*d] -> vt[(b*H + h)*d + dd][l] (row stride ld_vt), dtype preserved.
+int launch_transpose_v(const LaunchCtx& c, const void* v, void* vt, long long ld_vt, int B, int L, int H, int d,
+                       int f32);
+// Rotate q [B, L, H*d] into out (same layout) with the 3D-RoPE table.
+int launch_rope_apply(const LaunchCtx& c, const void* in, void* out, const RopeGeom& g, int B, int L, int H, int d,
+                      int f32);
+int launch_schedule(const LaunchCtx& c, float* ts, int steps);
+
+// RoPE table geometry for head_dim d on grid (Fg, Hg, Wg).
+inline RopeGeom rope_geom(const float2* tab, int Fg, int Hg, int Wg, int d) {
+  RopeGeom g;
+  const int dh = 2 * (d / 6);
+  const int df = d - 2 * dh;
+  g.tab = tab;
+  g.Fg = Fg;
+  g.Hg = Hg;
+  g.Wg = Wg;
+  g.nf = df / 2;
+  g.nh = dh / 2;
+  g.nw = dh / 2;
+  return g;
+}
+inline size_t rope_table_entries(int Fg, int Hg, int Wg, int d) {
+  RopeGeom g = rope_geom(nullptr, Fg, Hg, Wg, d);
+  return (size_t)Fg * g.nf + (size_t)Hg * g.nh + (size_t)Wg * g.nw;
+}
+
+}  // namespace wan
