@@ -112,6 +112,21 @@ class Clocks:
 
 # ---------------------------------------------------------------- CPU oracle baseline
 
+def blas_threads() -> int:
+    """Threads numpy's BLAS runs the oracle's matrix products on."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except ImportError:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return len(os.sched_getaffinity(0))
+
+
 def oracle_step_estimate(s, seed=0, rows_small=16, rows_large=48):
     """Time the fp64 oracle on a bounded sample of one block and extrapolate to a step.
 
@@ -120,7 +135,6 @@ def oracle_step_estimate(s, seed=0, rows_small=16, rows_large=48):
     at two row counts; block time = fixed + L * per_row; step = batch * blocks * block.
     """
     from oracle import wan_oracle as O
-    from threadpoolctl import threadpool_info
     one = s.replace(blocks=1)
     w = synth.make_weights(one, seed)
     inp = synth.make_inputs(one, seed)
@@ -139,7 +153,7 @@ def oracle_step_estimate(s, seed=0, rows_small=16, rows_large=48):
     fixed = max(times[rows_small] - rows_small * per_row, 0.0)
     block = fixed + one.tokens * per_row
     step = block * s.batch * s.blocks
-    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    threads = blas_threads()
     sample = (f"one {one.dim}-wide block, batch entry 0: full LN+QKV over {one.tokens} tokens plus "
               f"{rows_small} and {rows_large} query rows end to end ({sum(times.values()):.1f} s of CPU); "
               f"extrapolated x{s.batch} batch x{s.blocks} blocks")
@@ -287,6 +301,7 @@ def run_ours(a, s):
         "kernels": kernels,
     }
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        print(json.dumps({"partial": out}), file=sys.stderr, flush=True)
         step_s, threads, sample, spent = oracle_step_estimate(s)
         out["cpu_baseline"] = {"value": round(tokens_per_step / step_s, 3), "unit": UNIT, "cores": threads,
                                "kind": "oracle", "sample": sample, "cpu_seconds": round(spent, 1),

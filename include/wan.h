@@ -198,6 +198,17 @@ typedef struct wan_dit_weights {
 /* Bytes of workspace wan_dit_forward / wan_dit_guided_step / wan_sample need. */
 size_t wan_dit_workspace_size(const wan_dit_config* cfg);
 
+/* [Method] time conditioning: an MLP of Linear and SiLU layers on the sinusoidal time
+ * embedding, shared by all blocks, predicting the six modulation vectors.
+ * READING (pages silent on the exact form): s = [cos(1000 t w_k), sin(1000 t w_k)],
+ * w_k = 10000^(-k/(freq_dim/2)); e = t2(SiLU(t1(s))); e0 = m(SiLU(e)) -> [B, 6, D]
+ * (shift1, scale1, gate1, shift2, scale2, gate2); hm = hm(SiLU(e)) -> [B, 2, D]
+ * (head shift, scale).  t: fp32 DEVICE, t[b * t_stride]; e0, hm: fp32 outputs.
+ * Uses the t1/t2/m/hm weights of `w` only.  ws: >= wan_time_embed_workspace_size(cfg). */
+size_t wan_time_embed_workspace_size(const wan_dit_config* cfg);
+int wan_time_embed(const wan_dit_config* cfg, const wan_dit_weights* w, const float* t, int t_stride, float* e0,
+                   float* hm, void* ws, size_t ws_bytes, wan_stream_t stream);
+
 /* [Method] + [Code]: the DiT velocity prediction.  patchify -> `blocks` transformer
  * blocks (AdaLN-modulated self-attention with 3D RoPE, cross-attention to ctx_txt (and
  * decoupled ctx_img), AdaLN-modulated GELU FFN, gated residuals) -> head -> depatchify.

@@ -4,6 +4,9 @@ bf16 configurations: max |g - o| <= 3e-2 * RMS(o) and sum|g - o| / sum|o| <= 5e-
 fp32 configuration:  max_i |g_i - o_i| / max(|o_i|, RMS(o)) <= 1e-4 (relative error
 floored at the RMS so near-zero elements do not dominate).
 """
+import json
+import os
+
 import numpy as np
 
 BF16_MAX_ABS_OVER_RMS = 3e-2
@@ -30,8 +33,16 @@ def bf16_errors(g, o):
     return float(err.max() / rms), float(err.sum() / np.abs(o).sum())
 
 
+def _log(**rec):
+    path = os.environ.get("WAN_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(rec) + "\n")
+
+
 def assert_bf16_close(g, o, what=""):
     mx, mr = bf16_errors(g, o)
+    _log(what=what, kind="bf16", max_abs_over_rms=mx, mean_rel=mr, ok=bool(mx <= BF16_MAX_ABS_OVER_RMS and mr <= BF16_MEAN_REL))
     assert mx <= BF16_MAX_ABS_OVER_RMS and mr <= BF16_MEAN_REL, \
         f"{what}: max|err|/rms = {mx:.3e} (<= {BF16_MAX_ABS_OVER_RMS}), mean rel = {mr:.3e} (<= {BF16_MEAN_REL})"
     return mx, mr
@@ -48,6 +59,7 @@ def f32_error(g, o):
 
 def assert_f32_close(g, o, what="", tol=F32_MAX_REL):
     e = f32_error(g, o)
+    _log(what=what, kind="f32", max_rel=e, tol=tol, ok=bool(e <= tol))
     assert e <= tol, f"{what}: max rel err {e:.3e} > {tol}"
     return e
 

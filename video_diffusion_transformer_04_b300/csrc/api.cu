@@ -188,7 +188,7 @@ static int patchify_impl(const LaunchCtx& c, const float* latent, long long lat_
   EpiParams ep = epi_base(EPI_STORE, M, D, L, b, f32);
   ep.out = x;
   ep.ldo = D;
-  ep.out_f32 = 1;
+  ep.out_type = OUT_F32;
   if (f32) return proj(c, 1, A, 4LL * C, 4 * C, w, 4LL * C, 4 * C, M, D, 4 * C, 0, ep, "gemm_patchify");
   return proj(c, 0, A, 2 * kpad, (int)(2 * kpad), w, 4LL * C, 4 * C, M, D, (int)(2 * kpad), (int)(kpad / 64), ep,
               "gemm_patchify");
@@ -268,6 +268,18 @@ static int validate_weights(const wan_dit_config* cfg, const wan_dit_weights* w)
   return WAN_OK;
 }
 
+// s = sinusoid(t); e = t2(SiLU(t1(s))); e0 = m(SiLU(e)); hm = hm(SiLU(e)).
+static int time_embed_impl(const LaunchCtx& c, const wan_dit_config* cfg, const wan_dit_weights* w, const float* t,
+                           int t_stride, float* tsin, float* h1, float* e, float* e0, float* hm) {
+  const int f32 = cfg->dtype == WAN_F32;
+  const int B = cfg->batch, D = cfg->dim;
+  WAN_TRY(launch_sinusoid(c, t, t_stride, tsin, B, cfg->freq_dim));
+  WAN_TRY(launch_small_linear(c, tsin, w->t1_w, w->t1_b, f32, h1, B, D, cfg->freq_dim, 0, 1));
+  WAN_TRY(launch_small_linear(c, h1, w->t2_w, w->t2_b, f32, e, B, D, D, 0, 0));
+  WAN_TRY(launch_small_linear(c, e, w->m_w, w->m_b, f32, e0, B, 6 * D, D, 1, 0));
+  return launch_small_linear(c, e, w->hm_w, w->hm_b, f32, hm, B, 2 * D, D, 1, 0);
+}
+
 static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w, const float* latent,
                             long long lat_bstride, const float* t, int t_stride, const void* ctx_txt,
                             const void* ctx_img, float* v_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
@@ -292,11 +304,7 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
   // 3D RoPE table and the shared time embedding -> six modulation vectors per block.
   WAN_TRY(launch_rope_table(c, W.rope, Fg, Hg, Wg, hd, cfg->theta));
   const RopeGeom rg = rope_geom(W.rope, Fg, Hg, Wg, hd);
-  WAN_TRY(launch_sinusoid(c, t, t_stride, W.tsin, B, cfg->freq_dim));
-  WAN_TRY(launch_small_linear(c, W.tsin, w->t1_w, w->t1_b, f32, W.h1, B, D, cfg->freq_dim, 0, 1));
-  WAN_TRY(launch_small_linear(c, W.h1, w->t2_w, w->t2_b, f32, W.e, B, D, D, 0, 0));
-  WAN_TRY(launch_small_linear(c, W.e, w->m_w, w->m_b, f32, W.e0, B, 6 * D, D, 1, 0));
-  WAN_TRY(launch_small_linear(c, W.e, w->hm_w, w->hm_b, f32, W.hm, B, 2 * D, D, 1, 0));
+  WAN_TRY(time_embed_impl(c, cfg, w, t, t_stride, W.tsin, W.h1, W.e, W.e0, W.hm));
   {
     std::vector<const void*> mp(cfg->blocks);
     for (int i = 0; i < cfg->blocks; ++i) mp[i] = w->blocks[i].mod;
@@ -317,7 +325,8 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
       EpiParams ep = epi_base(EPI_QKV, M, 3 * D, L, bw.qkv_b, f32);
       ep.qk = W.qk;
       ep.ldqk = 2LL * D;
-      ep.qk_f32 = f32;
+      ep.qk_type = f32 ? OUT_F32 : OUT_F16;  // q, k feed the QK^T MMA in fp16
+      ep.vt_type = f32 ? OUT_F32 : OUT_BF16;
       ep.n_qk = 2 * D;
       ep.n_rot = 2 * D;
       ep.vt = W.vt;
@@ -336,6 +345,7 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
       a.o = W.o; a.ldo = D; a.o_col = 0;
       a.B = B; a.Lq = L; a.Lkv = L; a.H = H; a.head_dim = hd;
       a.tag = "attn_self";
+      a.qk_f16 = !f32;
       WAN_TRY(attend(c, f32, a));
     }
     {
@@ -353,7 +363,7 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
       EpiParams ep = epi_base(EPI_STORE, M, D, L, bw.cq_b, f32);
       ep.out = W.qc;
       ep.ldo = D;
-      ep.out_f32 = f32;
+      ep.out_type = f32 ? OUT_F32 : OUT_F16;
       WAN_TRY(proj(c, f32, W.y, D, D, bw.cq_w, D, D, M, D, D, 0, ep, "gemm_cross_q"));
     }
     for (int seg = 0; seg < (Li ? 2 : 1); ++seg) {
@@ -364,7 +374,8 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
       EpiParams ep = epi_base(EPI_QKV, B * Lk, 2 * D, Lk, seg ? bw.ckvi_b : bw.ckv_b, f32);
       ep.qk = kbuf;
       ep.ldqk = D;
-      ep.qk_f32 = f32;
+      ep.qk_type = f32 ? OUT_F32 : OUT_F16;
+      ep.vt_type = f32 ? OUT_F32 : OUT_BF16;
       ep.n_qk = D;
       ep.n_rot = 0;
       ep.vt = vbuf;
@@ -382,6 +393,7 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
       a.B = B; a.Lq = L; a.Lkv = Lk; a.H = H; a.head_dim = hd;
       a.accumulate = seg;
       a.tag = "attn_cross";
+      a.qk_f16 = !f32;
       WAN_TRY(attend(c, f32, a));
     }
     {
@@ -397,7 +409,7 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
       EpiParams ep = epi_base(EPI_GELU, M, Fh, L, bw.f1_b, f32);
       ep.out = W.h;
       ep.ldo = Fh;
-      ep.out_f32 = f32;
+      ep.out_type = f32 ? OUT_F32 : OUT_BF16;
       WAN_TRY(proj(c, f32, W.y, D, D, bw.f1_w, D, D, M, Fh, D, 0, ep, "gemm_ffn1_gelu"));
     }
     {
@@ -536,6 +548,7 @@ int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B,
   a.o = o; a.ldo = D;
   a.B = B; a.Lq = L; a.Lkv = L; a.H = H; a.head_dim = d;
   a.tag = "attn_self";
+  a.qk_f16 = apply_rope && !f32;  // rotated q, k are written in fp16
   return attend(c, f32, a);
 }
 
@@ -599,7 +612,7 @@ int wan_ffn(const void* y, const void* w1, const void* b1, const void* w2, const
   EpiParams e1 = epi_base(EPI_GELU, M, F, L, b1, f32);
   e1.out = h_ws;
   e1.ldo = F;
-  e1.out_f32 = f32;
+  e1.out_type = f32 ? OUT_F32 : OUT_BF16;
   WAN_TRY(proj(c, f32, y, D, D, w1, D, D, M, F, D, 0, e1, "gemm_ffn1_gelu"));
   EpiParams e2 = epi_base(EPI_RESID, M, D, L, b2, f32);
   e2.resid = x_inout;
@@ -632,7 +645,7 @@ int wan_linear(const void* x, const void* w, const void* b, void* out, int M, in
   } else {
     ep.out = out;
     ep.ldo = N;
-    ep.out_f32 = out_dtype == WAN_F32;
+    ep.out_type = out_dtype == WAN_F32 ? OUT_F32 : OUT_BF16;
   }
   return proj(c, f32, x, K, K, w, K, K, M, N, K, 0, ep, "gemm_linear");
 }
@@ -656,12 +669,12 @@ int wan_text_embed(const void* text, const void* w1, const void* b1, const void*
   EpiParams e1 = epi_base(EPI_GELU, M, D, Lt, b1, f32);
   e1.out = ws;
   e1.ldo = D;
-  e1.out_f32 = f32;
+  e1.out_type = f32 ? OUT_F32 : OUT_BF16;
   WAN_TRY(proj(c, f32, text, Ct, Ct, w1, Ct, Ct, M, D, Ct, 0, e1, "gemm_text1_gelu"));
   EpiParams e2 = epi_base(EPI_STORE, M, D, Lt, b2, f32);
   e2.out = ctx;
   e2.ldo = D;
-  e2.out_f32 = f32;
+  e2.out_type = f32 ? OUT_F32 : OUT_BF16;
   return proj(c, f32, ws, D, D, w2, D, D, M, D, D, 0, e2, "gemm_text2");
 }
 
@@ -680,6 +693,32 @@ int wan_cfg_euler_step(float* x, const void* v_cond, const void* v_uncond, long 
 size_t wan_dit_workspace_size(const wan_dit_config* cfg) {
   if (validate_cfg(cfg) != WAN_OK) return 0;
   return plan_forward(cfg, nullptr).bytes;
+}
+
+size_t wan_time_embed_workspace_size(const wan_dit_config* cfg) {
+  if (validate_cfg(cfg) != WAN_OK) return 0;
+  Bump bp(nullptr);
+  bp.take<float>((size_t)cfg->batch * cfg->freq_dim);
+  bp.take<float>((size_t)cfg->batch * cfg->dim);
+  bp.take<float>((size_t)cfg->batch * cfg->dim);
+  return (size_t)round_up((long long)bp.off, 1024);
+}
+
+int wan_time_embed(const wan_dit_config* cfg, const wan_dit_weights* w, const float* t, int t_stride, float* e0,
+                   float* hm, void* ws, size_t ws_bytes, wan_stream_t stream) {
+  WAN_TRY(validate_cfg(cfg));
+  if (!w || !w->t1_w || !w->t1_b || !w->t2_w || !w->t2_b || !w->m_w || !w->m_b || !w->hm_w || !w->hm_b || !t || !e0 ||
+      !hm || t_stride < 0)
+    return WAN_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < wan_time_embed_workspace_size(cfg) || (reinterpret_cast<uintptr_t>(ws) & 1023))
+    return WAN_ERR_WORKSPACE;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  Bump bp(ws);
+  float* tsin = bp.take<float>((size_t)cfg->batch * cfg->freq_dim);
+  float* h1 = bp.take<float>((size_t)cfg->batch * cfg->dim);
+  float* e = bp.take<float>((size_t)cfg->batch * cfg->dim);
+  return time_embed_impl(c, cfg, w, t, t_stride, tsin, h1, e, e0, hm);
 }
 
 int wan_dit_forward(const wan_dit_config* cfg, const wan_dit_weights* w, const float* latent, int latent_broadcast,

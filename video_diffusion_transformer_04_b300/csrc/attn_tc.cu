@@ -46,7 +46,7 @@ struct AttnParams {
   int accumulate;         // o += result (decoupled cross-attention)
 };
 
-template <int HD>
+template <int HD, bool QK_F16>
 __global__ void __launch_bounds__(320, 1)
     attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnParams p, int* status) {
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
-    constexpr uint32_t idS = make_idesc_bf16(128, Cfg::BKV);
+    constexpr uint32_t idS = QK_F16 ? make_idesc_f16(128, Cfg::BKV) : make_idesc_bf16(128, Cfg::BKV);
     constexpr uint32_t idO = make_idesc_bf16(128, HD);
     bool ok = mbar_wait(q_full, 0, status, kDevTimeoutAttn) && mbar_wait(&k_full[0], 0, status, kDevTimeoutAttn);
     auto issue_S = [&](int i, int ks) {
@@ -301,20 +301,20 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
-template <int HD>
+template <int HD, bool QK_F16>
 static int launch_attn(const LaunchCtx& c, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const AttnParams& p, int B, const char* tag) {
   using Cfg = AttnCfg<HD>;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_bf16_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(attn_bf16_tc_kernel<HD, QK_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::SMEM) != cudaSuccess)
       return WAN_ERR_CUDA;
     attr_set = true;
   }
   const long long grid = (long long)B * p.H * p.nq_pairs;
   count_launch(tag, c.stream, true);
-  attn_bf16_tc_kernel<HD><<<(unsigned)grid, Cfg::THREADS, Cfg::SMEM, c.stream>>>(tq, tk, tv, p, c.dev_status);
+  attn_bf16_tc_kernel<HD, QK_F16><<<(unsigned)grid, Cfg::THREADS, Cfg::SMEM, c.stream>>>(tq, tk, tv, p, c.dev_status);
   count_launch(tag, c.stream, false);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
@@ -324,10 +324,11 @@ int attention_bf16(const LaunchCtx& c, const AttnArgs& a) {
   if (a.Lq <= 0 || a.Lkv <= 0) return WAN_OK;
   const int HD = a.head_dim;
   CUtensorMap tq, tk, tv;
-  int st = make_tmap_3d(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.q_row_len, (uint64_t)a.Lq,
+  const CUtensorMapDataType qkt = a.qk_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  int st = make_tmap_3d(&tq, a.q, qkt, 2, (uint64_t)a.q_row_len, (uint64_t)a.Lq,
                         (uint64_t)a.B, (uint64_t)a.ldq * 2, (uint64_t)a.ldq * 2 * a.Lq, 64, 128);
   if (st != WAN_OK) return st;
-  st = make_tmap_3d(&tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.k_row_len, (uint64_t)a.Lkv,
+  st = make_tmap_3d(&tk, a.k, qkt, 2, (uint64_t)a.k_row_len, (uint64_t)a.Lkv,
                     (uint64_t)a.B, (uint64_t)a.ldk * 2, (uint64_t)a.ldk * 2 * a.Lkv, 64, 128);
   if (st != WAN_OK) return st;
   st = make_tmap_2d(&tv, a.vt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.Lkv,
@@ -346,7 +347,9 @@ int attention_bf16(const LaunchCtx& c, const AttnArgs& a) {
   p.o_col = a.o_col;
   p.accumulate = a.accumulate;
   const char* tag = a.tag ? a.tag : "attn";
-  return HD == 128 ? launch_attn<128>(c, tq, tk, tv, p, a.B, tag) : launch_attn<64>(c, tq, tk, tv, p, a.B, tag);
+  if (HD == 128)
+    return a.qk_f16 ? launch_attn<128, true>(c, tq, tk, tv, p, a.B, tag) : launch_attn<128, false>(c, tq, tk, tv, p, a.B, tag);
+  return a.qk_f16 ? launch_attn<64, true>(c, tq, tk, tv, p, a.B, tag) : launch_attn<64, false>(c, tq, tk, tv, p, a.B, tag);
 }
 
 }  // namespace wan

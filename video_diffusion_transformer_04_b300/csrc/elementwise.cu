@@ -359,9 +359,9 @@ int launch_transpose_v(const LaunchCtx& c, const void* v, void* vt, long long ld
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
 
-template <typename T>
-__global__ void rope_apply_kernel(const T* __restrict__ in, T* __restrict__ out, RopeGeom g, long long rows, int L,
-                                  int H, int d) {
+template <typename Tin, typename Tout>
+__global__ void rope_apply_kernel(const Tin* __restrict__ in, Tout* __restrict__ out, RopeGeom g, long long rows,
+                                  int L, int H, int d) {
   const long long pairs_per_row = (long long)H * d / 2;
   const long long total = rows * pairs_per_row;
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
@@ -369,21 +369,22 @@ __global__ void rope_apply_kernel(const T* __restrict__ in, T* __restrict__ out,
     const int pr = (int)(e - m * pairs_per_row);
     const int l = (int)(m % L);
     const int dd0 = (pr * 2) % d;
+    const long long i0 = m * H * d + 2 * pr;
     float v[2];
-    if constexpr (sizeof(T) == 4) {
-      v[0] = in[m * H * d + 2 * pr];
-      v[1] = in[m * H * d + 2 * pr + 1];
+    if constexpr (sizeof(Tin) == 4) {
+      v[0] = in[i0];
+      v[1] = in[i0 + 1];
     } else {
-      v[0] = bf2f(in[m * H * d + 2 * pr]);
-      v[1] = bf2f(in[m * H * d + 2 * pr + 1]);
+      v[0] = bf2f(in[i0]);
+      v[1] = bf2f(in[i0 + 1]);
     }
     epi_rope<2>(g, d, dd0, l, v);
-    if constexpr (sizeof(T) == 4) {
-      out[m * H * d + 2 * pr] = v[0];
-      out[m * H * d + 2 * pr + 1] = v[1];
+    if constexpr (sizeof(Tout) == 4) {
+      out[i0] = v[0];
+      out[i0 + 1] = v[1];
     } else {
-      out[m * H * d + 2 * pr] = __float2bfloat16_rn(v[0]);
-      out[m * H * d + 2 * pr + 1] = __float2bfloat16_rn(v[1]);
+      out[i0] = __float2half_rn(v[0]);
+      out[i0 + 1] = __float2half_rn(v[1]);
     }
   }
 }
@@ -396,13 +397,11 @@ int launch_rope_apply(const LaunchCtx& c, const void* in, void* out, const RopeG
   if (blocks > (long long)c.num_sms * 16) blocks = (long long)c.num_sms * 16;
   count_launch("rope_apply", c.stream, true);
   if (f32)
-    rope_apply_kernel<float><<<(unsigned)blocks, 256, 0, c.stream>>>(static_cast<const float*>(in),
-                                                                     static_cast<float*>(out), g, (long long)B * L, L,
-                                                                     H, d);
+    rope_apply_kernel<float, float><<<(unsigned)blocks, 256, 0, c.stream>>>(
+        static_cast<const float*>(in), static_cast<float*>(out), g, (long long)B * L, L, H, d);
   else
-    rope_apply_kernel<bf16><<<(unsigned)blocks, 256, 0, c.stream>>>(static_cast<const bf16*>(in),
-                                                                    static_cast<bf16*>(out), g, (long long)B * L, L, H,
-                                                                    d);
+    rope_apply_kernel<bf16, __half><<<(unsigned)blocks, 256, 0, c.stream>>>(
+        static_cast<const bf16*>(in), static_cast<__half*>(out), g, (long long)B * L, L, H, d);
   count_launch("rope_apply", c.stream, false);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }

@@ -4,6 +4,8 @@
 // over HBM is needed for them.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include "wan_common.cuh"
 
 namespace wan {
@@ -22,6 +24,9 @@ struct RopeGeom {
   int nf, nh, nw;     // rotation pairs per axis
 };
 
+// Storage types of epilogue outputs.
+enum OutType : int { OUT_BF16 = 0, OUT_F32 = 1, OUT_F16 = 2 };
+
 struct EpiParams {
   int kind;
   int M, N;
@@ -31,7 +36,7 @@ struct EpiParams {
   // EPI_STORE / EPI_GELU
   void* out;
   long long ldo;
-  int out_f32;
+  int out_type;  // OutType
   // EPI_RESID
   float* resid;
   long long ldr;
@@ -40,7 +45,8 @@ struct EpiParams {
   // EPI_QKV
   void* qk;
   long long ldqk;
-  int qk_f32;
+  int qk_type;  // OutType of q|k
+  int vt_type;  // OutType of v^T (OUT_BF16 or OUT_F32)
   int n_qk, n_rot;
   void* vt;            // [(b*H + h)*hd + dd] rows of ld_vt elements
   long long ld_vt;
@@ -56,33 +62,39 @@ __device__ __forceinline__ float epi_bias(const EpiParams& p, int n) {
   return bf2f(static_cast<const bf16*>(p.bias)[n]);
 }
 
-// Store CNT consecutive values (CNT % 4 == 0, 16-byte aligned destinations).
+// Store CNT consecutive values (CNT % 4 == 0, 16-byte aligned destinations for CNT >= 8).
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 p = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
 template <int CNT>
-__device__ __forceinline__ void epi_store_row(void* base, int is_f32, long long off, const float* v) {
-  if (is_f32) {
+__device__ __forceinline__ void epi_store_row(void* base, int type, long long off, const float* v) {
+  if (type == OUT_F32) {
     float4* d = reinterpret_cast<float4*>(static_cast<float*>(base) + off);
 #pragma unroll
     for (int i = 0; i < CNT / 4; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    return;
+  }
+  uint16_t* d = static_cast<uint16_t*>(base) + off;
+  const bool h = type == OUT_F16;
+  if constexpr (CNT % 8 == 0) {
+#pragma unroll
+    for (int i = 0; i < CNT / 8; ++i) {
+      uint4 u;
+      u.x = h ? pack_half2(v[8 * i + 0], v[8 * i + 1]) : pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+      u.y = h ? pack_half2(v[8 * i + 2], v[8 * i + 3]) : pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+      u.z = h ? pack_half2(v[8 * i + 4], v[8 * i + 5]) : pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+      u.w = h ? pack_half2(v[8 * i + 6], v[8 * i + 7]) : pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+      reinterpret_cast<uint4*>(d)[i] = u;
+    }
   } else {
-    bf16* d = static_cast<bf16*>(base) + off;
-    if constexpr (CNT % 8 == 0) {
 #pragma unroll
-      for (int i = 0; i < CNT / 8; ++i) {
-        uint4 u;
-        u.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-        u.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-        u.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-        u.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-        reinterpret_cast<uint4*>(d)[i] = u;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < CNT / 4; ++i) {
-        uint2 u;
-        u.x = pack_bf16x2(v[4 * i + 0], v[4 * i + 1]);
-        u.y = pack_bf16x2(v[4 * i + 2], v[4 * i + 3]);
-        reinterpret_cast<uint2*>(d)[i] = u;
-      }
+    for (int i = 0; i < CNT / 4; ++i) {
+      uint2 u;
+      u.x = h ? pack_half2(v[4 * i + 0], v[4 * i + 1]) : pack_bf16x2(v[4 * i + 0], v[4 * i + 1]);
+      u.y = h ? pack_half2(v[4 * i + 2], v[4 * i + 3]) : pack_bf16x2(v[4 * i + 2], v[4 * i + 3]);
+      reinterpret_cast<uint2*>(d)[i] = u;
     }
   }
 }
@@ -127,7 +139,7 @@ __device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int m, int n0
       for (int i = 0; i < CNT; ++i) v[i] = gelu_erf(v[i]);
       // fallthrough
     case EPI_STORE:
-      epi_store_row<CNT>(p.out, p.out_f32, (long long)m * p.ldo + n0, v);
+      epi_store_row<CNT>(p.out, p.out_type, (long long)m * p.ldo + n0, v);
       break;
     case EPI_RESID: {
       float4* x = reinterpret_cast<float4*>(p.resid + (long long)m * p.ldr + n0);
@@ -147,13 +159,13 @@ __device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int m, int n0
     case EPI_QKV: {
       if (n0 < p.n_qk) {
         if (n0 < p.n_rot) epi_rope<CNT>(p.rope, p.head_dim, n0 % p.head_dim, l, v);
-        epi_store_row<CNT>(p.qk, p.qk_f32, (long long)m * p.ldqk + n0, v);
+        epi_store_row<CNT>(p.qk, p.qk_type, (long long)m * p.ldqk + n0, v);
       } else {
         const int c = n0 - p.n_qk;
         const int h = c / p.head_dim;
         const int dd0 = c - h * p.head_dim;
         const long long row0 = ((long long)b * p.heads + h) * p.head_dim + dd0;
-        if (p.qk_f32) {
+        if (p.vt_type == OUT_F32) {
           float* vt = static_cast<float*>(p.vt);
 #pragma unroll
           for (int i = 0; i < CNT; ++i) vt[(row0 + i) * p.ld_vt + l] = v[i];

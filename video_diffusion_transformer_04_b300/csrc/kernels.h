@@ -41,6 +41,7 @@ struct AttnArgs {
   int o_col;
   int B, Lq, Lkv, H, head_dim;
   int accumulate;  // o += result
+  int qk_f16;      // bf16 path: q and k are fp16 (else bf16); v^T and o are bf16
   const char* tag; // profiler label of the launch
 };
 int attention_bf16(const LaunchCtx& c, const AttnArgs& a);
@@ -65,7 +66,8 @@ int launch_block_mods(const LaunchCtx& c, const float* e0, const void* const* mo
 // v [B, L, H*d] -> vt[(b*H + h)*d + dd][l] (row stride ld_vt), dtype preserved.
 int launch_transpose_v(const LaunchCtx& c, const void* v, void* vt, long long ld_vt, int B, int L, int H, int d,
                        int f32);
-// Rotate q [B, L, H*d] into out (same layout) with the 3D-RoPE table.
+// Rotate q [B, L, H*d] into out (same layout) with the 3D-RoPE table; bf16 input is
+// written out in fp16, fp32 stays fp32.
 int launch_rope_apply(const LaunchCtx& c, const void* in, void* out, const RopeGeom& g, int B, int L, int H, int d,
                       int f32);
 int launch_schedule(const LaunchCtx& c, float* ts, int steps);

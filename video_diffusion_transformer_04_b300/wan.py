@@ -76,6 +76,8 @@ _SIGS = {
     "wan_text_embed": (I, [P, P, P, P, P, P, I, I, I, I, I, P, SZ, P]),
     "wan_cfg_euler_step": (I, [P, P, P, LL, F, F, I, P]),
     "wan_dit_workspace_size": (SZ, [C.POINTER(wan_dit_config)]),
+    "wan_time_embed_workspace_size": (SZ, [C.POINTER(wan_dit_config)]),
+    "wan_time_embed": (I, [C.POINTER(wan_dit_config), C.POINTER(wan_dit_weights), P, I, P, P, P, SZ, P]),
     "wan_dit_forward": (I, [C.POINTER(wan_dit_config), C.POINTER(wan_dit_weights), P, I, P, P, P, P, P, SZ, P]),
     "wan_dit_guided_step": (I, [C.POINTER(wan_dit_config), C.POINTER(wan_dit_weights), P, P, F, P, P, P, P, SZ,
                                 P]),
@@ -203,6 +205,13 @@ def wan_dit_workspace_size(cfg: wan_dit_config) -> int:
     return lib.wan_dit_workspace_size(C.byref(cfg))
 
 
+def wan_time_embed(cfg, weights, t, e0, hm, t_stride=1, stream=None):
+    ws = torch.empty(lib.wan_time_embed_workspace_size(C.byref(cfg)) + 1024, dtype=torch.uint8, device=t.device)
+    ws = ws[(-ws.data_ptr()) % 1024:]
+    _check(lib.wan_time_embed(C.byref(cfg), C.byref(weights), _p(t), t_stride, _p(e0), _p(hm), _p(ws),
+                              ws.numel(), _stream(stream)), "wan_time_embed")
+
+
 def wan_dit_forward(cfg, weights, latent, t, ctx_txt, ctx_img, v_out, ws, latent_broadcast=False, stream=None):
     _check(lib.wan_dit_forward(C.byref(cfg), C.byref(weights), _p(latent), 1 if latent_broadcast else 0, _p(t),
                                _p(ctx_txt), _p(ctx_img), _p(v_out), _p(ws), ws.numel() * ws.element_size(),
@@ -277,6 +286,13 @@ class DiT:
         t = self.tensors
         wan_text_embed(text, t["txt1_w"], t["txt1_b"], t["txt2_w"], t["txt2_b"], ctx, ws, stream)
         return ctx
+
+    def time_embed(self, t, stream=None):
+        s = self.shape
+        e0 = torch.empty(s.batch, 6, s.dim, dtype=torch.float32, device=t.device)
+        hm = torch.empty(s.batch, 2, s.dim, dtype=torch.float32, device=t.device)
+        wan_time_embed(self.cfg, self.weights_c, t, e0, hm, 1 if t.numel() > 1 else 0, stream)
+        return e0, hm
 
     def forward(self, latent, t, ctx_txt, ctx_img=None, latent_broadcast=False, v_out=None, stream=None):
         s = self.shape
