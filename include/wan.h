@@ -150,6 +150,28 @@ int wan_text_embed(const void* text, const void* w1, const void* b1, const void*
                    void* ctx, int B, int Lt, int Ct, int D, int dtype, void* ws, size_t ws_bytes,
                    wan_stream_t stream);
 
+/* ------------------------------------------------------------------ text projection without allocation
+ * No counterpart in the paper: a library convenience.  Same computation and result as
+ * wan_text_embed, for callers that cannot allocate device memory (a host that owns the
+ * whole allocator and passes only fixed input/output buffers, or a latency-critical path
+ * where an allocation may stall or fail).  The scratch (the hidden activations between
+ * the two linear layers) lives in a static device array of
+ * wan_text_embed_noalloc_max_bytes() = 16 MiB inside libwan, held by every GPU that
+ * loads the library until the process exits; nothing is allocated per call.
+ *   - Sizes whose scratch, wan_text_embed_workspace_size(B, Lt, D, dtype), exceeds the
+ *     maximum are rejected with WAN_ERR_WORKSPACE before anything is launched (bf16: up
+ *     to B*Lt*D = 8 Mi elements).
+ *   - The first call on a device resolves the array's device address (once per device);
+ *     make that first call before capturing a stream into a CUDA graph.
+ *   - Every call on a device shares the one array, which keeps the last call's contents
+ *     (the scratch is fully written before it is read, so nothing needs clearing).
+ *     Calls whose work overlaps on the GPU (different streams, concurrent graphs) race on
+ *     the array: serialise them.
+ * Arguments as for wan_text_embed, without ws / ws_bytes. */
+int wan_text_embed_noalloc(const void* text, const void* w1, const void* b1, const void* w2, const void* b2,
+                           void* ctx, int B, int Lt, int Ct, int D, int dtype, wan_stream_t stream);
+size_t wan_text_embed_noalloc_max_bytes(void);
+
 /* ------------------------------------------------------------------ CFG + Euler
  * [Code] noise_pred = uncond + s * (cond - uncond); [Sampler 4.4] x <- x + v * dt, with
  * t running from 1 (noise) to 0 (data) and dt = t_next - t:

@@ -74,6 +74,8 @@ _SIGS = {
     "wan_linear": (I, [P, P, P, P, I, I, I, I, P, I, I, I, P]),
     "wan_text_embed_workspace_size": (SZ, [I, I, I, I]),
     "wan_text_embed": (I, [P, P, P, P, P, P, I, I, I, I, I, P, SZ, P]),
+    "wan_text_embed_noalloc": (I, [P, P, P, P, P, P, I, I, I, I, I, P]),
+    "wan_text_embed_noalloc_max_bytes": (SZ, []),
     "wan_cfg_euler_step": (I, [P, P, P, LL, F, F, I, P]),
     "wan_dit_workspace_size": (SZ, [C.POINTER(wan_dit_config)]),
     "wan_time_embed_workspace_size": (SZ, [C.POINTER(wan_dit_config)]),
@@ -194,6 +196,18 @@ def wan_text_embed(text, w1, b1, w2, b2, ctx, ws, stream=None):
     _check(lib.wan_text_embed(_p(text), _p(w1), _p(b1), _p(w2), _p(b2), _p(ctx), B, Lt, Ct, D,
                               dtype_code(text.dtype), _p(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "wan_text_embed")
+
+
+def wan_text_embed_noalloc(text, w1, b1, w2, b2, ctx, stream=None):
+    """wan_text_embed with libwan's static scratch: no allocation by libwan or here."""
+    B, Lt, Ct = text.shape
+    D = w1.shape[0]
+    _check(lib.wan_text_embed_noalloc(_p(text), _p(w1), _p(b1), _p(w2), _p(b2), _p(ctx), B, Lt, Ct, D,
+                                      dtype_code(text.dtype), _stream(stream)), "wan_text_embed_noalloc")
+
+
+def wan_text_embed_noalloc_max_bytes() -> int:
+    return lib.wan_text_embed_noalloc_max_bytes()
 
 
 def wan_cfg_euler_step(x, v_cond, v_uncond, guide_scale, dt, stream=None):
