@@ -57,7 +57,10 @@ enum wan_status_code {
   WAN_ERR_WORKSPACE = -5    /* ws NULL, misaligned or smaller than required */
 };
 
-enum wan_dtype { WAN_BF16 = 0, WAN_F32 = 1 };
+/* Storage types.  WAN_F16 (fp16) is accepted only where an entry point says so: for the
+ * q and k operands of the attention calls next to bf16 v and o (fp16 keeps 3 more
+ * mantissa bits in the logits q.k than bf16), and as the output of wan_linear. */
+enum wan_dtype { WAN_BF16 = 0, WAN_F32 = 1, WAN_F16 = 2 };
 
 /* Epilogues of wan_linear: y = x W^T + b followed by ... */
 enum wan_epilogue {
@@ -103,24 +106,28 @@ int wan_adaln_modulate(const float* x, const float* shift, const float* scale, v
  * (d - 4*floor(d/6), 2*floor(d/6), 2*floor(d/6)); adjacent pairs (2m, 2m+1) of part a
  * rotate by pos_a * theta^(-2j/d_a), pos = the token's (f, i, j) on the grid
  * (Fg, Hg, Wg), Fg*Hg*Wg == L.
- * q, k, v, o: [B, L, H, d] (dtype).  apply_rope = 0 treats q and k as already rotated.
+ * v, o: [B, L, H, d] in dtype; q, k: [B, L, H, d] in qk_dtype (= dtype, or WAN_F16 with
+ * dtype WAN_BF16).  apply_rope = 0 treats q and k as already rotated.  With dtype
+ * WAN_BF16 the rotated q and k enter the QK^T product in fp16.
  * ws: >= wan_attn_workspace_size(...).  d must be 64 or 128 (bf16 path); d <= 128 and
  * even (fp32 path). */
 size_t wan_attn_workspace_size(int B, int L, int H, int d, int dtype);
 int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B, int L, int H, int d,
-                    int Fg, int Hg, int Wg, float theta, int apply_rope, int dtype, void* ws,
-                    size_t ws_bytes, wan_stream_t stream);
+                    int Fg, int Hg, int Wg, float theta, int apply_rope, int dtype, int qk_dtype,
+                    void* ws, size_t ws_bytes, wan_stream_t stream);
 
 /* ------------------------------------------------------------------ cross-attention
  * [Method] text conditioning by cross-attention; [I2V] decoupled cross-attention to the
  * CLIP image context: o = softmax(q kt^T/sqrt(d)) vt + softmax(q ki^T/sqrt(d)) vi
  * (the second term only when ki != NULL).
- * q, o: [B, L, H, d]; kt, vt: [B, Lt, H, d]; ki, vi: [B, Li, H, d] or NULL (dtype).
+ * o: [B, L, H, d]; vt: [B, Lt, H, d]; vi: [B, Li, H, d] or NULL (dtype).
+ * q: [B, L, H, d]; kt: [B, Lt, H, d]; ki: [B, Li, H, d] or NULL (qk_dtype: dtype, or
+ * WAN_F16 with dtype WAN_BF16).
  * ws: >= wan_cross_attn_workspace_size(...). */
 size_t wan_cross_attn_workspace_size(int B, int Lt, int Li, int H, int d, int dtype);
 int wan_cross_attn(const void* q, const void* kt, const void* vt, const void* ki, const void* vi,
-                   void* o, int B, int L, int Lt, int Li, int H, int d, int dtype, void* ws,
-                   size_t ws_bytes, wan_stream_t stream);
+                   void* o, int B, int L, int Lt, int Li, int H, int d, int dtype, int qk_dtype,
+                   void* ws, size_t ws_bytes, wan_stream_t stream);
 
 /* ------------------------------------------------------------------ FFN
  * FFN sub-layer with gated residual: x += gate[b] * (W2 GELU(W1 y + b1) + b2).
@@ -134,9 +141,10 @@ int wan_ffn(const void* y, const void* w1, const void* b1, const void* w2, const
 /* ------------------------------------------------------------------ linear
  * One projection y = x W^T + b with an epilogue (enum wan_epilogue); the GEMM under every
  * projection of the block.  x: [M, K] (dtype); w: [N, K]; b: [N] or NULL (dtype).
- * WAN_EPI_STORE / WAN_EPI_GELU write out [M, N] in out_dtype (WAN_BF16 only with
- * dtype WAN_BF16).  WAN_EPI_RESIDUAL accumulates into the fp32 out [M, N] with the
- * optional fp32 gate [M / rows_per_gate, N].  Needs K % 8 == 0, N % 32 == 0. */
+ * WAN_EPI_STORE / WAN_EPI_GELU write out [M, N] in out_dtype (WAN_BF16 or WAN_F16 only
+ * with dtype WAN_BF16).  WAN_EPI_RESIDUAL accumulates into the fp32 out [M, N] with the
+ * optional fp32 gate [M / rows_per_gate, N] (out_dtype WAN_F32).  Needs K % 8 == 0,
+ * N % 32 == 0. */
 int wan_linear(const void* x, const void* w, const void* b, void* out, int M, int N, int K,
                int epilogue, const float* gate, int rows_per_gate, int dtype, int out_dtype,
                wan_stream_t stream);

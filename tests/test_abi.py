@@ -69,6 +69,15 @@ def test_host_validation_rejects_bad_arguments(wanlib):
     g.argtypes = [C.c_void_p] * 4 + [C.c_int] * 4 + [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p]
     assert g(None, None, None, None, 8, 64, 64, 0, None, 0, 0, 0, None) == -1
     assert g(None, None, None, None, 8, 64, 64, 9, None, 0, 0, 0, None) == -1
+    # fp16 storage is an output type of the bf16 GEMM only, and never the residual's type
+    assert g(1 << 12, 1 << 12, None, 1 << 12, 8, 64, 64, 0, None, 0, 1, 2, None) == -2
+    assert g(1 << 12, 1 << 12, None, 1 << 12, 8, 64, 64, 2, None, 0, 0, 2, None) == -2
+    h = wanlib.wan_cross_attn
+    h.argtypes = [C.c_void_p] * 6 + [C.c_int] * 8 + [C.c_void_p, C.c_size_t, C.c_void_p]
+    # q/k in fp16 are accepted only next to bf16 v/o; unknown codes are invalid
+    assert h(None, None, None, None, None, None, 1, 8, 8, 0, 1, 64, 1, 2, None, 0, None) == -2
+    assert h(None, None, None, None, None, None, 1, 8, 8, 0, 1, 64, 0, 5, None, 0, None) == -1
+    assert h(None, None, None, None, None, None, 1, 8, 8, 0, 1, 64, 0, 2, None, 0, None) == -1  # NULL q
 
 
 def test_dit_workspace_size_arithmetic():

@@ -12,7 +12,7 @@ import synth
 from tests.parity import assert_bf16_close, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
-BF, F32 = torch.bfloat16, torch.float32
+BF, F16, F32 = torch.bfloat16, torch.float16, torch.float32
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
@@ -50,9 +50,12 @@ def test_block_composed_from_ops(wan, n):
     wan.wan_adaln_modulate(x, sh1, sc1, y)
     check("y1", y)
 
-    qkv = torch.empty(L, 3 * D, dtype=BF, device=dev)
-    wan.wan_linear(y.view(L, D), blk["qkv_w"], blk["qkv_b"], qkv)
-    q, k, v = (qkv[:, i * D:(i + 1) * D].contiguous().view(1, L, H, d) for i in range(3))
+    # q and k in fp16 (as the fused forward stores them for the QK^T product), v in bf16
+    qk = torch.empty(L, 2 * D, dtype=F16, device=dev)
+    wan.wan_linear(y.view(L, D), blk["qkv_w"][:2 * D], blk["qkv_b"][:2 * D], qk)
+    v = torch.empty(1, L, H, d, dtype=BF, device=dev)
+    wan.wan_linear(y.view(L, D), blk["qkv_w"][2 * D:], blk["qkv_b"][2 * D:], v.view(L, D))
+    q, k = (qk[:, i * D:(i + 1) * D].contiguous().view(1, L, H, d) for i in range(2))
     o = torch.empty(1, L, H, d, dtype=BF, device=dev)
     aws = torch.empty(wan.wan_attn_workspace_size(1, L, H, d, wan.WAN_BF16) + 1024, dtype=torch.uint8, device=dev)
     aws = aws[(-aws.data_ptr()) % 1024:]
@@ -62,7 +65,7 @@ def test_block_composed_from_ops(wan, n):
     check("x_sa", x)
 
     wan.wan_adaln_modulate(x, None, None, y)
-    qc = torch.empty(1, L, H, d, dtype=BF, device=dev)
+    qc = torch.empty(1, L, H, d, dtype=F16, device=dev)
     wan.wan_linear(y.view(L, D), blk["cq_w"], blk["cq_b"], qc.view(L, D))
     if s.text_dim:
         ctx = m.text_embed(to_dev(inp["text"], BF))
@@ -71,9 +74,11 @@ def test_block_composed_from_ops(wan, n):
     Lt = s.text_len
 
     def kv_of(c, wname, bname, Lk):
-        kvb = torch.empty(Lk, 2 * D, dtype=BF, device=dev)
-        wan.wan_linear(c.view(Lk, D), blk[wname], blk[bname], kvb)
-        return kvb[:, :D].contiguous().view(1, Lk, H, d), kvb[:, D:].contiguous().view(1, Lk, H, d)
+        kb = torch.empty(1, Lk, H, d, dtype=F16, device=dev)
+        vb = torch.empty(1, Lk, H, d, dtype=BF, device=dev)
+        wan.wan_linear(c.view(Lk, D), blk[wname][:D], blk[bname][:D], kb.view(Lk, D))
+        wan.wan_linear(c.view(Lk, D), blk[wname][D:], blk[bname][D:], vb.view(Lk, D))
+        return kb, vb
 
     kt, vt = kv_of(ctx[:1], "ckv_w", "ckv_b", Lt)
     ki = vi = None

@@ -132,13 +132,15 @@ def _attn_inputs(seed, B, L, H, d, bf):
 
 @pytest.mark.parametrize("B,grid,H,d", ATTN_CASES)
 @pytest.mark.parametrize("rope", [True, False])
-def test_attn_rope3d_bf16(wan, B, grid, H, d, rope):
+@pytest.mark.parametrize("qkt", ["bf16", "f16"])
+def test_attn_rope3d_bf16(wan, B, grid, H, d, rope, qkt):
     L = grid[0] * grid[1] * grid[2]
-    q, k, v = _attn_inputs(6, B, L, H, d, True)     # q, k ~ N(0, 1): peaky softmax
+    q, k, v = _attn_inputs(6, B, L, H, d, True)     # q, k ~ N(0, 1): peaky softmax (bf16-exact values)
     o = torch.full((B, L, H, d), float("nan"), dtype=BF, device="cuda")
     ws = torch.empty(wan.wan_attn_workspace_size(B, L, H, d, wan.WAN_BF16) + 1024, dtype=torch.uint8, device="cuda")
     ws = ws[(-ws.data_ptr()) % 1024:]
-    wan.wan_attn_rope3d(to_dev(q, BF), to_dev(k, BF), to_dev(v, BF), o, grid, apply_rope=rope, ws=ws)
+    QK = BF if qkt == "bf16" else torch.float16
+    wan.wan_attn_rope3d(to_dev(q, QK), to_dev(k, QK), to_dev(v, BF), o, grid, apply_rope=rope, ws=ws)
     wan.wan_sync_status()
     pos = O.token_positions(grid)
     for b in range(B):
@@ -181,7 +183,8 @@ def test_attn_full_size_sampled_rows(wan):
 # ---------------------------------------------------------------- cross-attention
 
 @pytest.mark.parametrize("B,L,Lt,Li,H,d", [(2, 130, 512, 257, 2, 128), (1, 48, 16, 0, 2, 64), (1, 1, 1, 1, 1, 128)])
-def test_cross_attn_bf16(wan, B, L, Lt, Li, H, d):
+@pytest.mark.parametrize("qkt", ["bf16", "f16"])
+def test_cross_attn_bf16(wan, B, L, Lt, Li, H, d, qkt):
     q = rb(synth.normal(9, "ca.q", (B, L, H, d)))
     kt = rb(synth.normal(9, "ca.kt", (B, Lt, H, d)))
     vt = rb(synth.normal(9, "ca.vt", (B, Lt, H, d)))
@@ -191,7 +194,8 @@ def test_cross_attn_bf16(wan, B, L, Lt, Li, H, d):
     ws = torch.empty(wan.wan_cross_attn_workspace_size(B, Lt, Li, H, d, wan.WAN_BF16) + 1024, dtype=torch.uint8,
                      device="cuda")
     ws = ws[(-ws.data_ptr()) % 1024:]
-    wan.wan_cross_attn(to_dev(q, BF), to_dev(kt, BF), to_dev(vt, BF), to_dev(ki, BF) if Li else None,
+    QK = BF if qkt == "bf16" else torch.float16
+    wan.wan_cross_attn(to_dev(q, QK), to_dev(kt, QK), to_dev(vt, BF), to_dev(ki, QK) if Li else None,
                        to_dev(vi, BF) if Li else None, o, ws)
     wan.wan_sync_status()
     for b in range(B):

@@ -171,6 +171,14 @@ static int attend(const LaunchCtx& c, int f32, const AttnArgs& a) {
 
 static int check_dtype(int dtype) { return (dtype == WAN_BF16 || dtype == WAN_F32) ? WAN_OK : WAN_ERR_INVALID_ARG; }
 
+// q/k storage of an attention call: the call's dtype, or fp16 alongside bf16 v/o.
+static int check_qk_dtype(int dtype, int qk_dtype) {
+  if (qk_dtype == dtype) return WAN_OK;
+  if (dtype == WAN_BF16 && qk_dtype == WAN_F16) return WAN_OK;
+  return (qk_dtype == WAN_BF16 || qk_dtype == WAN_F32 || qk_dtype == WAN_F16) ? WAN_ERR_UNSUPPORTED
+                                                                               : WAN_ERR_INVALID_ARG;
+}
+
 // ------------------------------------------------------------------ patchify
 static long long patch_kpad(int C, int f32) { return f32 ? 4LL * C : round_up(4LL * C, 64); }
 
@@ -511,8 +519,10 @@ size_t wan_attn_workspace_size(int B, int L, int H, int d, int dtype) {
 }
 
 int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B, int L, int H, int d, int Fg, int Hg,
-                    int Wg, float theta, int apply_rope, int dtype, void* ws, size_t ws_bytes, wan_stream_t stream) {
+                    int Wg, float theta, int apply_rope, int dtype, int qk_dtype, void* ws, size_t ws_bytes,
+                    wan_stream_t stream) {
   WAN_TRY(check_dtype(dtype));
+  WAN_TRY(check_qk_dtype(dtype, qk_dtype));
   const int f32 = dtype == WAN_F32;
   if (!q || !k || !v || !o || B <= 0 || L <= 0 || H <= 0 || d <= 0) return WAN_ERR_INVALID_ARG;
   if (apply_rope && (Fg <= 0 || Hg <= 0 || Wg <= 0 || (long long)Fg * Hg * Wg != L)) return WAN_ERR_INVALID_ARG;
@@ -533,8 +543,9 @@ int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B,
   if (apply_rope) {
     WAN_TRY(launch_rope_table(c, tab, Fg, Hg, Wg, d, theta));
     const RopeGeom g = rope_geom(tab, Fg, Hg, Wg, d);
-    WAN_TRY(launch_rope_apply(c, q, qr, g, B, L, H, d, f32));
-    WAN_TRY(launch_rope_apply(c, k, kr, g, B, L, H, d, f32));
+    const int in_type = f32 ? OUT_F32 : (qk_dtype == WAN_F16 ? OUT_F16 : OUT_BF16);
+    WAN_TRY(launch_rope_apply(c, q, qr, g, B, L, H, d, in_type));
+    WAN_TRY(launch_rope_apply(c, k, kr, g, B, L, H, d, in_type));
     qa = qr;
     ka = kr;
   }
@@ -548,7 +559,7 @@ int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B,
   a.o = o; a.ldo = D;
   a.B = B; a.Lq = L; a.Lkv = L; a.H = H; a.head_dim = d;
   a.tag = "attn_self";
-  a.qk_f16 = apply_rope && !f32;  // rotated q, k are written in fp16
+  a.qk_f16 = !f32 && (apply_rope || qk_dtype == WAN_F16);  // rotated q, k are written in fp16
   return attend(c, f32, a);
 }
 
@@ -562,8 +573,10 @@ size_t wan_cross_attn_workspace_size(int B, int Lt, int Li, int H, int d, int dt
 }
 
 int wan_cross_attn(const void* q, const void* kt, const void* vt, const void* ki, const void* vi, void* o, int B,
-                   int L, int Lt, int Li, int H, int d, int dtype, void* ws, size_t ws_bytes, wan_stream_t stream) {
+                   int L, int Lt, int Li, int H, int d, int dtype, int qk_dtype, void* ws, size_t ws_bytes,
+                   wan_stream_t stream) {
   WAN_TRY(check_dtype(dtype));
+  WAN_TRY(check_qk_dtype(dtype, qk_dtype));
   const int f32 = dtype == WAN_F32;
   if (!q || !kt || !vt || !o || B <= 0 || L <= 0 || Lt <= 0 || Li < 0 || H <= 0 || d <= 0) return WAN_ERR_INVALID_ARG;
   if (Li > 0 && (!ki || !vi)) return WAN_ERR_INVALID_ARG;
@@ -593,6 +606,7 @@ int wan_cross_attn(const void* q, const void* kt, const void* vt, const void* ki
     a.B = B; a.Lq = L; a.Lkv = Lk; a.H = H; a.head_dim = d;
     a.accumulate = seg;
     a.tag = "attn_cross";
+    a.qk_f16 = qk_dtype == WAN_F16;
     WAN_TRY(attend(c, f32, a));
   }
   return WAN_OK;
@@ -625,12 +639,13 @@ int wan_ffn(const void* y, const void* w1, const void* b1, const void* w2, const
 int wan_linear(const void* x, const void* w, const void* b, void* out, int M, int N, int K, int epilogue,
                const float* gate, int rows_per_gate, int dtype, int out_dtype, wan_stream_t stream) {
   WAN_TRY(check_dtype(dtype));
-  WAN_TRY(check_dtype(out_dtype));
+  if (out_dtype != WAN_BF16 && out_dtype != WAN_F32 && out_dtype != WAN_F16) return WAN_ERR_INVALID_ARG;
   const int f32 = dtype == WAN_F32;
   if (!x || !w || !out || M <= 0 || N <= 0 || K <= 0) return WAN_ERR_INVALID_ARG;
   if (epilogue != WAN_EPI_STORE && epilogue != WAN_EPI_GELU && epilogue != WAN_EPI_RESIDUAL) return WAN_ERR_INVALID_ARG;
   if (gate && rows_per_gate <= 0) return WAN_ERR_INVALID_ARG;
   if (f32 && out_dtype != WAN_F32) return WAN_ERR_UNSUPPORTED;
+  if (epilogue == WAN_EPI_RESIDUAL && out_dtype != WAN_F32) return WAN_ERR_UNSUPPORTED;
   if (N % 32 || K % 8 || !aligned16(x) || !aligned16(w) || !aligned16(out) || (gate && !aligned16(gate)))
     return WAN_ERR_UNSUPPORTED;
   LaunchCtx c;
@@ -645,7 +660,7 @@ int wan_linear(const void* x, const void* w, const void* b, void* out, int M, in
   } else {
     ep.out = out;
     ep.ldo = N;
-    ep.out_type = out_dtype == WAN_F32 ? OUT_F32 : OUT_BF16;
+    ep.out_type = out_dtype == WAN_F32 ? OUT_F32 : (out_dtype == WAN_F16 ? OUT_F16 : OUT_BF16);
   }
   return proj(c, f32, x, K, K, w, K, K, M, N, K, 0, ep, "gemm_linear");
 }

@@ -1,6 +1,8 @@
 // Bandwidth-bound passes of the DiT step: LayerNorm + AdaLN modulation, fused CFG +
 // Euler update, the patch gather feeding the patchify GEMM, and the small kernels of
 // the time embedding, RoPE table and layout changes.
+#include <type_traits>
+
 #include "kernels.h"
 
 namespace wan {
@@ -374,6 +376,9 @@ __global__ void rope_apply_kernel(const Tin* __restrict__ in, Tout* __restrict__
     if constexpr (sizeof(Tin) == 4) {
       v[0] = in[i0];
       v[1] = in[i0 + 1];
+    } else if constexpr (std::is_same<Tin, __half>::value) {
+      v[0] = __half2float(in[i0]);
+      v[1] = __half2float(in[i0 + 1]);
     } else {
       v[0] = bf2f(in[i0]);
       v[1] = bf2f(in[i0 + 1]);
@@ -390,15 +395,18 @@ __global__ void rope_apply_kernel(const Tin* __restrict__ in, Tout* __restrict__
 }
 
 int launch_rope_apply(const LaunchCtx& c, const void* in, void* out, const RopeGeom& g, int B, int L, int H, int d,
-                      int f32) {
+                      int in_type) {
   const long long total = (long long)B * L * H * d / 2;
   if (total <= 0) return WAN_OK;
   long long blocks = (total + 255) / 256;
   if (blocks > (long long)c.num_sms * 16) blocks = (long long)c.num_sms * 16;
   count_launch("rope_apply", c.stream, true);
-  if (f32)
+  if (in_type == OUT_F32)
     rope_apply_kernel<float, float><<<(unsigned)blocks, 256, 0, c.stream>>>(
         static_cast<const float*>(in), static_cast<float*>(out), g, (long long)B * L, L, H, d);
+  else if (in_type == OUT_F16)
+    rope_apply_kernel<__half, __half><<<(unsigned)blocks, 256, 0, c.stream>>>(
+        static_cast<const __half*>(in), static_cast<__half*>(out), g, (long long)B * L, L, H, d);
   else
     rope_apply_kernel<bf16, __half><<<(unsigned)blocks, 256, 0, c.stream>>>(
         static_cast<const bf16*>(in), static_cast<__half*>(out), g, (long long)B * L, L, H, d);

@@ -123,6 +123,32 @@ __device__ __forceinline__ void epi_rope(const RopeGeom& g, int head_dim, int dd
   (void)head_dim;
 }
 
+// Gated-residual update values of row m, columns n0..n0+CNT-1: v <- gate[b, n] * (v + bias[n])
+// (gate NULL: 1).  Rows at or past M (a tile's ragged tail) get 0 and read no gate.
+template <int CNT>
+__device__ __forceinline__ void epi_resid_values(const EpiParams& p, int m, int n0, float* v) {
+  if (m >= p.M) {
+#pragma unroll
+    for (int i = 0; i < CNT; ++i) v[i] = 0.f;
+    return;
+  }
+  if (p.bias) {
+#pragma unroll
+    for (int i = 0; i < CNT; ++i) v[i] += epi_bias(p, n0 + i);
+  }
+  if (p.gate) {
+    const float* g = p.gate + (long long)(m / p.rows_per_batch) * p.ld_gate + n0;
+#pragma unroll
+    for (int i = 0; i < CNT / 4; ++i) {
+      const float4 gg = *reinterpret_cast<const float4*>(g + 4 * i);
+      v[4 * i] *= gg.x;
+      v[4 * i + 1] *= gg.y;
+      v[4 * i + 2] *= gg.z;
+      v[4 * i + 3] *= gg.w;
+    }
+  }
+}
+
 // Apply the epilogue to values v[0..CNT) of row m, columns n0..n0+CNT-1 (all valid;
 // n0 % CNT == 0 and the chunk never straddles a section or head boundary).
 template <int CNT>

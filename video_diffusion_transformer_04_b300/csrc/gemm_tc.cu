@@ -10,7 +10,13 @@
 //               row per thread), bias/GELU/RoPE/gated residual/layout, global stores
 // The accumulator is double-buffered in TMEM (2 x BN columns), so the epilogue of tile
 // i overlaps the main loop of tile i+1.
+// The gated residual x += gate * (acc + bias) never reads x into the SM: each warp
+// stages its 32 x 32 fp32 chunk in shared memory (128-byte swizzle, conflict-free for
+// one-row-per-thread writes) and a TMA reduce-add applies it to x in L2, so the
+// read-modify-write of the fp32 residual stream moves whole lines and leaves no load
+// latency in the epilogue.
 #include <cstdio>
+#include <cstring>
 
 #include "epilogue.cuh"
 #include "kernels.h"
@@ -26,19 +32,23 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
   static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int EPI_STAGE_BYTES = 4 * 2 * 32 * 32 * 4;  // 4 warps x 2 buffers x [32][32] fp32
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + BAR_BYTES + 1024;
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
+  static_assert(SMEM <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
 template <int BN>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const EpiParams ep, int M, int N, int K, int kb_period, int* status) {
+                        const __grid_constant__ CUtensorMap tmR, const EpiParams ep, int M, int N, int K,
+                        int kb_period, int* status) {
   using Cfg = GemmCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
+  uint8_t* epi_stage = smem + Cfg::STAGES * Cfg::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi_stage + Cfg::EPI_STAGE_BYTES);
   uint64_t* empty = full + Cfg::STAGES;
   uint64_t* tfull = empty + Cfg::STAGES;
   uint64_t* tempty = tfull + 2;
@@ -140,20 +150,45 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp >= 2) {
     // ---------------------------------------------------------------- epilogue
     const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad + 32) belong to this warp
+    const bool tma_resid = ep.kind == EPI_RESID;
+    float* stage = reinterpret_cast<float*>(epi_stage + quad * (2 * 32 * 32 * 4));  // 2 x [32][32], 1 KB aligned
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t nstaged = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int mb = tile / num_n, nb = tile - (tile / num_n) * num_n;
       if (!mbar_wait_warp(&tfull[acc], acc_phase, status, kDevTimeoutGemm)) break;
       tc_fence_after();
-      const int row = mb * Cfg::BM + quad * 32 + lane;
+      const int row0 = mb * Cfg::BM + quad * 32;
+      const int row = row0 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(taddr + c * 32, r);
         const int n0 = nb * BN + c * 32;
-        if (row < M && n0 < N) {
+        if (tma_resid) {
+          if (row0 < M && n0 < N) {  // warp-uniform; rows past M are clipped by the TMA
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            epi_resid_values<32>(ep, row, n0, v);
+            float* buf = stage + (nstaged & 1) * (32 * 32);
+            if (lane == 0) bulk_wait_group_read<1>();  // the reduce that last read `buf` is done
+            __syncwarp();
+            float4* dst = reinterpret_cast<float4*>(buf + lane * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j ^ (lane & 7)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_2d(&tmR, buf, n0, row0);
+              bulk_commit_group();
+            }
+            ++nstaged;
+          }
+        } else if (row < M && n0 < N) {
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
@@ -165,6 +200,8 @@ __global__ void __launch_bounds__(192, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (tma_resid && lane == 0) bulk_wait_group_all();  // reduces finished before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -174,8 +211,8 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 template <int BN>
-static int launch_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb, const EpiParams& ep,
-                       int M, int N, int K, int kb_period, const char* tag) {
+static int launch_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr,
+                       const EpiParams& ep, int M, int N, int K, int kb_period, const char* tag) {
   using Cfg = GemmCfg<BN>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -187,7 +224,7 @@ static int launch_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensor
   const int tiles = ((M + 127) / 128) * ((N + BN - 1) / BN);
   const int grid = tiles < c.num_sms ? tiles : c.num_sms;
   count_launch(tag, c.stream, true);
-  gemm_bf16_tc_kernel<BN><<<grid, 192, Cfg::SMEM, c.stream>>>(ta, tb, ep, M, N, K, kb_period, c.dev_status);
+  gemm_bf16_tc_kernel<BN><<<grid, 192, Cfg::SMEM, c.stream>>>(ta, tb, tr, ep, M, N, K, kb_period, c.dev_status);
   count_launch(tag, c.stream, false);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
@@ -203,10 +240,18 @@ int gemm_bf16(const LaunchCtx& c, const bf16* A, long long lda, int a_cols, cons
   st = make_tmap_2d(&tb, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)b_cols, (uint64_t)N, (uint64_t)ldb * 2,
                     64, (uint32_t)bn);
   if (st != WAN_OK) return st;
+  CUtensorMap tr;
+  memset(&tr, 0, sizeof(tr));
+  if (ep.kind == EPI_RESID) {  // the fp32 residual x [M, N] (row stride ldr), 32 x 32 boxes
+    if (ep.ldr % 4 != 0) return WAN_ERR_UNSUPPORTED;
+    st = make_tmap_2d(&tr, ep.resid, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)N, (uint64_t)M,
+                      (uint64_t)ep.ldr * 4, 32, 32);
+    if (st != WAN_OK) return st;
+  }
   switch (bn) {
-    case 256: return launch_gemm<256>(c, ta, tb, ep, M, N, K, kb_period, tag);
-    case 128: return launch_gemm<128>(c, ta, tb, ep, M, N, K, kb_period, tag);
-    default: return launch_gemm<64>(c, ta, tb, ep, M, N, K, kb_period, tag);
+    case 256: return launch_gemm<256>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
+    case 128: return launch_gemm<128>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
+    default: return launch_gemm<64>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
   }
 }
 

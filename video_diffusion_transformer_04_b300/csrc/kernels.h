@@ -66,10 +66,10 @@ int launch_block_mods(const LaunchCtx& c, const float* e0, const void* const* mo
 // v [B, L, H*d] -> vt[(b*H + h)*d + dd][l] (row stride ld_vt), dtype preserved.
 int launch_transpose_v(const LaunchCtx& c, const void* v, void* vt, long long ld_vt, int B, int L, int H, int d,
                        int f32);
-// Rotate q [B, L, H*d] into out (same layout) with the 3D-RoPE table; bf16 input is
-// written out in fp16, fp32 stays fp32.
+// Rotate q [B, L, H*d] into out (same layout) with the 3D-RoPE table.  in_type (OutType):
+// bf16 or fp16 input is written out in fp16, fp32 stays fp32.
 int launch_rope_apply(const LaunchCtx& c, const void* in, void* out, const RopeGeom& g, int B, int L, int H, int d,
-                      int f32);
+                      int in_type);
 int launch_schedule(const LaunchCtx& c, float* ts, int steps);
 
 // RoPE table geometry for head_dim d on grid (Fg, Hg, Wg).

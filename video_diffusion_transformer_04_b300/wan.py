@@ -17,7 +17,7 @@ import torch
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libwan.so")
 
 WAN_OK, WAN_ERR_INVALID_ARG, WAN_ERR_UNSUPPORTED, WAN_ERR_CUDA, WAN_ERR_TIMEOUT, WAN_ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
-WAN_BF16, WAN_F32 = 0, 1
+WAN_BF16, WAN_F32, WAN_F16 = 0, 1, 2
 WAN_EPI_STORE, WAN_EPI_GELU, WAN_EPI_RESIDUAL = 0, 1, 2
 
 
@@ -67,9 +67,9 @@ _SIGS = {
     "wan_patchify": (I, [P, P, P, P, I, I, I, I, I, I, I, P, SZ, P]),
     "wan_adaln_modulate": (I, [P, P, P, P, I, I, I, F, I, P]),
     "wan_attn_workspace_size": (SZ, [I, I, I, I, I]),
-    "wan_attn_rope3d": (I, [P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, SZ, P]),
+    "wan_attn_rope3d": (I, [P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, P, SZ, P]),
     "wan_cross_attn_workspace_size": (SZ, [I, I, I, I, I, I]),
-    "wan_cross_attn": (I, [P, P, P, P, P, P, I, I, I, I, I, I, I, P, SZ, P]),
+    "wan_cross_attn": (I, [P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, SZ, P]),
     "wan_ffn": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, P]),
     "wan_linear": (I, [P, P, P, P, I, I, I, I, P, I, I, I, P]),
     "wan_text_embed_workspace_size": (SZ, [I, I, I, I]),
@@ -119,7 +119,13 @@ def _check(st, where):
 
 
 def dtype_code(t: torch.dtype) -> int:
-    return WAN_F32 if t == torch.float32 else WAN_BF16
+    if t == torch.float32:
+        return WAN_F32
+    if t == torch.float16:
+        return WAN_F16
+    if t == torch.bfloat16:
+        return WAN_BF16
+    raise ValueError(f"libwan has no storage type for {t}")
 
 
 # ---------------------------------------------------------------- per-op entry points
@@ -156,8 +162,8 @@ def wan_attn_workspace_size(B, L, H, d, dtype):
 def wan_attn_rope3d(q, k, v, o, grid, theta=10000.0, apply_rope=True, ws=None, stream=None):
     B, L, H, d = q.shape
     _check(lib.wan_attn_rope3d(_p(q), _p(k), _p(v), _p(o), B, L, H, d, grid[0], grid[1], grid[2], theta,
-                               1 if apply_rope else 0, dtype_code(q.dtype), _p(ws), ws.numel() * ws.element_size(),
-                               _stream(stream)), "wan_attn_rope3d")
+                               1 if apply_rope else 0, dtype_code(v.dtype), dtype_code(q.dtype), _p(ws),
+                               ws.numel() * ws.element_size(), _stream(stream)), "wan_attn_rope3d")
 
 
 def wan_cross_attn_workspace_size(B, Lt, Li, H, d, dtype):
@@ -168,8 +174,9 @@ def wan_cross_attn(q, kt, vt, ki, vi, o, ws, stream=None):
     B, L, H, d = q.shape
     Lt = kt.shape[1]
     Li = ki.shape[1] if ki is not None else 0
-    _check(lib.wan_cross_attn(_p(q), _p(kt), _p(vt), _p(ki), _p(vi), _p(o), B, L, Lt, Li, H, d, dtype_code(q.dtype),
-                              _p(ws), ws.numel() * ws.element_size(), _stream(stream)), "wan_cross_attn")
+    _check(lib.wan_cross_attn(_p(q), _p(kt), _p(vt), _p(ki), _p(vi), _p(o), B, L, Lt, Li, H, d, dtype_code(vt.dtype),
+                              dtype_code(q.dtype), _p(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "wan_cross_attn")
 
 
 def wan_ffn(y, w1, b1, w2, b2, gate, x_inout, h_ws, stream=None):
