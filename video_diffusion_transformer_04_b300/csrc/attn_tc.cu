@@ -9,9 +9,14 @@
 //   warp 0      TMA: Q once, then K and V^T tiles into 2-deep rings
 //   warp 1      tcgen05.mma from one thread: S_i = Q_i K^T (both operands in smem),
 //               O_i += P_i V (P from TMEM, V^T tile from smem), ping-ponging the tiles
-//   warps 2..9  softmax, one warpgroup per query tile, one thread per query row: fp32
+//   warps 4..11 softmax, one warpgroup per query tile, one thread per query row: fp32
 //               running max and sum, exp2 on the MUFU unit, lazy rescale of O in TMEM
 //               only when the running max grows by more than 2^8, final 1/l and store.
+// The first warpgroup (TMA, MMA, two idle warps) gives registers to the softmax
+// warpgroups (setmaxnreg), which keep a whole 128-column score row in registers.
+// Per score element the softmax issues half an FFMA2 (scale and max subtraction on
+// packed pairs), one MUFU ex2, half a bf16x2 pack, half an FADD2 (row sum) and half a
+// 3-input max; the ragged-tile mask runs only on the last key tile.
 // V arrives transposed ([d, keys], keys contiguous) so every MMA operand is K-major.
 // Ragged tails: keys past Lkv are zero-filled by TMA and masked to -inf; query rows
 // past Lq are computed on zero rows and not stored.
@@ -32,7 +37,12 @@ struct AttnCfg {
   static constexpr int SMEM_TILES = 2 * Q_BYTES + 2 * K_BYTES + 2 * V_BYTES;
   static constexpr int SMEM = SMEM_TILES + 256 + 1024;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 384;
+  // setmaxnreg split of the 384 x 168 registers the CTA launches with:
+  // 128 x PRODUCER_REGS + 256 x SOFTMAX_REGS <= 384 x 168.
+  static constexpr int PRODUCER_REGS = 56;
+  static constexpr int SOFTMAX_REGS = 224;
+  static_assert(128 * PRODUCER_REGS + 256 * SOFTMAX_REGS <= 384 * 168, "register split");
 };
 
 struct AttnParams {
@@ -47,7 +57,7 @@ struct AttnParams {
 };
 
 template <int HD, bool QK_F16>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnParams p, int* status) {
   using Cfg = AttnCfg<HD>;
@@ -99,6 +109,8 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
+  if (warp < 4) {
+  regs_dec<Cfg::PRODUCER_REGS>();
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
     tma_prefetch_desc(&tmQ);
@@ -191,35 +203,46 @@ __global__ void __launch_bounds__(320, 1)
       const unsigned long long t0 = globaltimer_ns();
       while (!mbar_test(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
     }
-  } else if (warp >= 2) {
+  }
+  } else {
     // ---------------------------------------------------------------- softmax
-    const int i = (warp - 2) >> 2;   // query tile of this warpgroup
+    regs_inc<Cfg::SOFTMAX_REGS>();
+    const int i = (warp - 4) >> 2;   // query tile of this warpgroup
     const int quad = warp & 3;       // TMEM lane quadrant of this warp
     if (i < ntile) {
       const uint32_t tS = tmem_base + ((uint32_t)(quad * 32) << 16) + i * 256;
       const uint32_t tO = tS + 128;
       const float sl2 = p.scale_log2;
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
       float m_used = -INFINITY;  // running max of the scaled logits (log2 units)
       float l_sum = 0.f;
       bool ok = true;
       for (int j = 0; j < nkv; ++j) {
         if (!mbar_wait_warp(&s_full[i], j & 1, status, kDevTimeoutAttn)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sr[4][32];
+        uint32_t sr[Cfg::BKV];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+        for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tS + c * 32, sr + c * 32);
+        tmem_wait_ld();
         const int valid = p.Lkv - j * Cfg::BKV;  // >= 1
-        float mt = -INFINITY;
+        if (valid < Cfg::BKV) {                  // ragged last key tile: mask keys >= Lkv
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int e = 0; e < Cfg::BKV; ++e)
+            if (e >= valid) sr[e] = __float_as_uint(-INFINITY);
+        }
+        // Row max over the tile: four independent chains of 3-input max.
+        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float s = __uint_as_float(sr[c][e]);
-            if (c * 32 + e >= valid) s = -INFINITY;
-            sr[c][e] = __float_as_uint(s);
-            mt = fmaxf(mt, s);
-          }
-        mt *= sl2;
+        for (int e = 4; e < Cfg::BKV - 4; e += 8) {
+          mx0 = fmax3(mx0, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
+          mx2 = fmax3(mx2, __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
+          mx3 = fmax3(mx3, __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
+        }
+        mx0 = fmax3(mx0, __uint_as_float(sr[Cfg::BKV - 4]), __uint_as_float(sr[Cfg::BKV - 3]));
+        mx1 = fmax3(mx1, __uint_as_float(sr[Cfg::BKV - 2]), __uint_as_float(sr[Cfg::BKV - 1]));
+        const float mt = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
         // Lazy rescale: a row moves its reference max only when the tile max exceeds it
         // by more than 8 (a factor 256 in the exponentials).  The O update is done by the
         // whole warp (tcgen05.ld/st are warp-collective), with alpha = 1 for rows that
@@ -238,21 +261,32 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
         if (need) m_used = mt;
-        float rs = 0.f;
+        // p = 2^(s * scale - m): packed pairs through FFMA2, exp2 on MUFU, bf16x2 into the
+        // first half of each 32-column chunk's registers (dead once read), row sum in
+        // four FADD2 accumulators on the fp32 values.
+        const uint64_t negm = f2_pack(-m_used, -m_used);
+        uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * e]), sl2, -m_used));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * e + 1]), sl2, -m_used));
-            pk[e] = pack_bf16x2(p0, p1);
-            const float2 q = unpack_bf16x2(pk[e]);
-            rs += q.x + q.y;
+            const uint64_t sp = f2_pack(__uint_as_float(sr[c * 32 + 2 * e]), __uint_as_float(sr[c * 32 + 2 * e + 1]));
+            const float2 t = f2_unpack(f2_fma(sp, sl2x2, negm));
+            const float p0 = ex2_approx(t.x), p1 = ex2_approx(t.y);
+            sr[c * 32 + e] = pack_bf16x2(p0, p1);
+            const uint64_t pp = f2_pack(p0, p1);
+            switch (e & 3) {
+              case 0: acc0 = f2_add(acc0, pp); break;
+              case 1: acc1 = f2_add(acc1, pp); break;
+              case 2: acc2 = f2_add(acc2, pp); break;
+              default: acc3 = f2_add(acc3, pp); break;
+            }
           }
-          tmem_st16(tS + c * 16, pk);
+          tmem_st16_nowait(tS + c * 16, sr + c * 32);
         }
-        l_sum += rs;
+        tmem_wait_st();
+        const float2 rs = f2_unpack(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)));
+        l_sum += rs.x + rs.y;
         tc_fence_before();
         mbar_arrive(&p_ready[i]);
       }
