@@ -20,6 +20,8 @@
 // V arrives transposed ([d, keys], keys contiguous) so every MMA operand is K-major.
 // Ragged tails: keys past Lkv are zero-filled by TMA and masked to -inf; query rows
 // past Lq are computed on zero rows and not stored.
+#include <type_traits>
+
 #include "kernels.h"
 #include "wan_common.cuh"
 
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
-      mbar_init(&p_ready[s], 128);
+      mbar_init(&p_ready[s], 4);  // one arrival per softmax warp
     }
     mbar_init(drain, 1);
     fence_barrier_init();
@@ -151,23 +153,29 @@ __global__ void __launch_bounds__(384, 1)
     constexpr uint32_t idS = QK_F16 ? make_idesc_f16(128, Cfg::BKV) : make_idesc_bf16(128, Cfg::BKV);
     constexpr uint32_t idO = make_idesc_bf16(128, HD);
     bool ok = mbar_wait(q_full, 0, status, kDevTimeoutAttn) && mbar_wait(&k_full[0], 0, status, kDevTimeoutAttn);
+    // Descriptor low words of every operand buffer, computed once: the issuing thread
+    // shares its SM sub-partition with two softmax warps, so each MMA costs only an add.
+    const uint32_t q_lo0 = sdesc_sw128_lo(smem_u32(sQ)), q_lo1 = sdesc_sw128_lo(smem_u32(sQ + Cfg::Q_BYTES));
+    const uint32_t k_lo0 = sdesc_sw128_lo(smem_u32(sK)), k_lo1 = sdesc_sw128_lo(smem_u32(sK + Cfg::K_BYTES));
+    const uint32_t v_lo0 = sdesc_sw128_lo(smem_u32(sV)), v_lo1 = sdesc_sw128_lo(smem_u32(sV + Cfg::V_BYTES));
     auto issue_S = [&](int i, int ks) {
-      const uint32_t qa = smem_u32(sQ + i * Cfg::Q_BYTES);
-      const uint32_t ka = smem_u32(sK + ks * Cfg::K_BYTES);
+      const uint32_t qa = i ? q_lo1 : q_lo0;
+      const uint32_t ka = ks ? k_lo1 : k_lo0;
+      const uint32_t d = tmem_base + i * 256;
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * Cfg::Q_BOX + (kk & 3) * 32;
-        tc_mma_ss(tmem_base + i * 256, make_sdesc_sw128(qa + off), make_sdesc_sw128(ka + off), idS,
-                  kk > 0 ? 1u : 0u);
+        const uint32_t off = ((kk >> 2) * Cfg::Q_BOX + (kk & 3) * 32) >> 4;
+        tc_mma_ss_lo(d, qa + off, ka + off, idS, kk > 0 ? 1u : 0u);
       }
     };
     auto issue_PV = [&](int i, int vs, uint32_t acc) {
-      const uint32_t va = smem_u32(sV + vs * Cfg::V_BYTES);
+      const uint32_t va = vs ? v_lo1 : v_lo0;
+      const uint32_t d = tmem_base + i * 256 + 128;
+      const uint32_t pa = tmem_base + i * 256;
 #pragma unroll
       for (int kk = 0; kk < Cfg::BKV / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * Cfg::V_BOX + (kk & 3) * 32;
-        tc_mma_ts(tmem_base + i * 256 + 128, tmem_base + i * 256 + kk * 8, make_sdesc_sw128(va + off), idO,
-                  (acc | (uint32_t)kk) != 0 ? 1u : 0u);
+        const uint32_t off = ((kk >> 2) * Cfg::V_BOX + (kk & 3) * 32) >> 4;
+        tc_mma_ts_lo(d, pa + kk * 8, va + off, idO, (acc | (uint32_t)kk) != 0 ? 1u : 0u);
       }
     };
     if (ok) {
@@ -217,61 +225,41 @@ __global__ void __launch_bounds__(384, 1)
       float m_used = -INFINITY;  // running max of the scaled logits (log2 units)
       float l_sum = 0.f;
       bool ok = true;
-      for (int j = 0; j < nkv; ++j) {
-        if (!mbar_wait_warp(&s_full[i], j & 1, status, kDevTimeoutAttn)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t sr[Cfg::BKV];
+      uint32_t sr[Cfg::BKV];
+      // S row of this thread -> sr (keys >= Lkv of a ragged last tile set to -inf).
+      auto load_scores = [&](int valid) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tS + c * 32, sr + c * 32);
         tmem_wait_ld();
-        const int valid = p.Lkv - j * Cfg::BKV;  // >= 1
-        if (valid < Cfg::BKV) {                  // ragged last key tile: mask keys >= Lkv
+        if (valid < Cfg::BKV) {
 #pragma unroll
           for (int e = 0; e < Cfg::BKV; ++e)
             if (e >= valid) sr[e] = __float_as_uint(-INFINITY);
         }
-        // Row max over the tile: four independent chains of 3-input max.
-        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
-#pragma unroll
-        for (int e = 4; e < Cfg::BKV - 4; e += 8) {
-          mx0 = fmax3(mx0, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
-          mx1 = fmax3(mx1, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
-          mx2 = fmax3(mx2, __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
-          mx3 = fmax3(mx3, __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
-        }
-        mx0 = fmax3(mx0, __uint_as_float(sr[Cfg::BKV - 4]), __uint_as_float(sr[Cfg::BKV - 3]));
-        mx1 = fmax3(mx1, __uint_as_float(sr[Cfg::BKV - 2]), __uint_as_float(sr[Cfg::BKV - 1]));
-        const float mt = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
-        // Lazy rescale: a row moves its reference max only when the tile max exceeds it
-        // by more than 8 (a factor 256 in the exponentials).  The O update is done by the
-        // whole warp (tcgen05.ld/st are warp-collective), with alpha = 1 for rows that
-        // keep their max.
-        const bool need = mt > m_used + 8.0f;
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
-          const float alpha = need ? ex2_approx(m_used - mt) : 1.0f;
-          l_sum *= alpha;
-#pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t orr[32];
-            tmem_ld32(tO + c * 32, orr);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-            tmem_st32(tO + c * 32, orr);
-          }
-        }
-        if (need) m_used = mt;
-        // p = 2^(s * scale - m): packed pairs through FFMA2, exp2 on MUFU, bf16x2 into the
-        // first half of each 32-column chunk's registers (dead once read), row sum in
-        // four FADD2 accumulators on the fp32 values.
-        const uint64_t negm = f2_pack(-m_used, -m_used);
+      };
+      // p = 2^(s * scale - m) on packed pairs (FFMA2, MUFU ex2), written as bf16x2 into
+      // the first half of each 32-column chunk's registers (dead once read); row sum in
+      // FADD2 accumulators on the fp32 values.  TRACK also returns the row max of s from
+      // the same reads (3-input max chains), off the exp dependency chain.
+      auto exp_pass = [&](auto track, float m, float& rowsum) -> float {
+        constexpr bool TRACK = decltype(track)::value;
+        const uint64_t negm = f2_pack(-m, -m);
         uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const uint64_t sp = f2_pack(__uint_as_float(sr[c * 32 + 2 * e]), __uint_as_float(sr[c * 32 + 2 * e + 1]));
-            const float2 t = f2_unpack(f2_fma(sp, sl2x2, negm));
+            const float s0 = __uint_as_float(sr[c * 32 + 2 * e]), s1 = __uint_as_float(sr[c * 32 + 2 * e + 1]);
+            if constexpr (TRACK) {
+              switch (e & 3) {
+                case 0: mx0 = fmax3(mx0, s0, s1); break;
+                case 1: mx1 = fmax3(mx1, s0, s1); break;
+                case 2: mx2 = fmax3(mx2, s0, s1); break;
+                default: mx3 = fmax3(mx3, s0, s1); break;
+              }
+            }
+            const float2 t = f2_unpack(f2_fma(f2_pack(s0, s1), sl2x2, negm));
             const float p0 = ex2_approx(t.x), p1 = ex2_approx(t.y);
             sr[c * 32 + e] = pack_bf16x2(p0, p1);
             const uint64_t pp = f2_pack(p0, p1);
@@ -282,13 +270,64 @@ __global__ void __launch_bounds__(384, 1)
               default: acc3 = f2_add(acc3, pp); break;
             }
           }
-          tmem_st16_nowait(tS + c * 16, sr + c * 32);
         }
-        tmem_wait_st();
         const float2 rs = f2_unpack(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)));
-        l_sum += rs.x + rs.y;
+        rowsum = rs.x + rs.y;
+        return fmax3(mx0, mx1, fmaxf(mx2, mx3));
+      };
+      for (int j = 0; j < nkv; ++j) {
+        if (!mbar_wait_warp(&s_full[i], j & 1, status, kDevTimeoutAttn)) { ok = false; break; }
+        tc_fence_after();
+        const int valid = p.Lkv - j * Cfg::BKV;  // >= 1
+        load_scores(valid);
+        float rowsum;
+        if (j == 0) {
+          // First key tile: the reference max is this tile's row max.
+          float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+          float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+#pragma unroll
+          for (int e = 4; e < Cfg::BKV - 4; e += 8) {
+            mx0 = fmax3(mx0, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
+            mx2 = fmax3(mx2, __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
+            mx3 = fmax3(mx3, __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
+          }
+          mx0 = fmax3(mx0, __uint_as_float(sr[Cfg::BKV - 4]), __uint_as_float(sr[Cfg::BKV - 3]));
+          mx1 = fmax3(mx1, __uint_as_float(sr[Cfg::BKV - 2]), __uint_as_float(sr[Cfg::BKV - 1]));
+          m_used = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+          exp_pass(std::false_type{}, m_used, rowsum);
+        } else {
+          // Lazy rescale: exponentiate against the current reference max and track the
+          // tile max on the way.  Only when some row's tile max exceeds its reference by
+          // more than 8 (a factor 256 in the exponentials) does the warp move those rows'
+          // reference, rescale their O and sum (alpha = 1 for the other rows: the
+          // tcgen05.ld/st are warp-collective), reload S and redo the exponentials.
+          const float mt = exp_pass(std::true_type{}, m_used, rowsum) * sl2;
+          const bool need = mt > m_used + 8.0f;
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ex2_approx(m_used - mt) : 1.0f;
+            l_sum *= alpha;
+            if (need) m_used = mt;
+#pragma unroll 1
+            for (int c = 0; c < HD / 32; ++c) {
+              uint32_t orr[32];
+              tmem_ld32(tO + c * 32, orr);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+              tmem_st32(tO + c * 32, orr);
+            }
+            load_scores(valid);
+            exp_pass(std::false_type{}, m_used, rowsum);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_st16_nowait(tS + c * 16, sr + c * 32);
+        tmem_wait_st();
+        l_sum += rowsum;
+        // One arrival per warp: the warp's TMEM stores are complete and ordered before it.
         tc_fence_before();
-        mbar_arrive(&p_ready[i]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_ready[i]);
       }
       if (ok && mbar_wait_warp(&s_full[i], nkv & 1, status, kDevTimeoutAttn)) {
         tc_fence_after();
