@@ -109,8 +109,9 @@ int wan_adaln_modulate(const float* x, const float* shift, const float* scale, v
  * v, o: [B, L, H, d] in dtype; q, k: [B, L, H, d] in qk_dtype (= dtype, or WAN_F16 with
  * dtype WAN_BF16).  apply_rope = 0 treats q and k as already rotated.  With dtype
  * WAN_BF16 the rotated q and k enter the QK^T product in fp16.
- * ws: >= wan_attn_workspace_size(...).  d must be 64 or 128 (bf16 path); d <= 128 and
- * even (fp32 path). */
+ * ws (the rotated q and k): >= wan_attn_workspace_size(...) bytes, 1024-byte aligned;
+ * unused (may be NULL) when apply_rope = 0.  d must be 64 or 128 (bf16 path); d <= 128
+ * and even (fp32 path). */
 size_t wan_attn_workspace_size(int B, int L, int H, int d, int dtype);
 int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B, int L, int H, int d,
                     int Fg, int Hg, int Wg, float theta, int apply_rope, int dtype, int qk_dtype,
@@ -123,7 +124,8 @@ int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B,
  * o: [B, L, H, d]; vt: [B, Lt, H, d]; vi: [B, Li, H, d] or NULL (dtype).
  * q: [B, L, H, d]; kt: [B, Lt, H, d]; ki: [B, Li, H, d] or NULL (qk_dtype: dtype, or
  * WAN_F16 with dtype WAN_BF16).
- * ws: >= wan_cross_attn_workspace_size(...). */
+ * ws, ws_bytes: unused (wan_cross_attn_workspace_size returns 0; q, k, v are read in
+ * place), kept so a caller can pass the same workspace to every attention call. */
 size_t wan_cross_attn_workspace_size(int B, int Lt, int Li, int H, int d, int dtype);
 int wan_cross_attn(const void* q, const void* kt, const void* vt, const void* ki, const void* vi,
                    void* o, int B, int L, int Lt, int Li, int H, int d, int dtype, int qk_dtype,

@@ -205,32 +205,27 @@ static int patchify_impl(const LaunchCtx& c, const float* latent, long long lat_
 // ------------------------------------------------------------------ forward workspace plan
 struct FwdWs {
   float* x;
-  void *y, *qk, *vt, *o, *qc, *kc, *vct, *kci, *vcit, *h, *patchA;
+  void *y, *qkv, *o, *qc, *kvc, *kvci, *h, *patchA;
   float *tsin, *h1, *e, *e0, *hm, *mods;
-  float2* rope;
+  float* rope;  // RoPE pair frequencies [head_dim / 2]
   size_t bytes;
 };
-
-static long long vt_ld(int L) { return round_up(L, 8); }
 
 static FwdWs plan_forward(const wan_dit_config* cfg, void* ws) {
   const int f32 = cfg->dtype == WAN_F32;
   const size_t es = f32 ? 4 : 2;
-  const long long B = cfg->batch, D = cfg->dim, H = cfg->heads, hd = cfg->head_dim;
+  const long long B = cfg->batch, D = cfg->dim, hd = cfg->head_dim;
   const long long L = (long long)cfg->frames * (cfg->height / 2) * (cfg->width / 2);
   const long long M = B * L;
   Bump bp(ws);
   FwdWs w;
   w.x = bp.take<float>(M * D);
   w.y = bp.take<uint8_t>(M * D * es);
-  w.qk = bp.take<uint8_t>(M * 2 * D * es);
-  w.vt = bp.take<uint8_t>(B * H * hd * vt_ld((int)L) * es);
+  w.qkv = bp.take<uint8_t>(M * 3 * D * es);  // rows q | k | v
   w.o = bp.take<uint8_t>(M * D * es);
   w.qc = bp.take<uint8_t>(M * D * es);
-  w.kc = bp.take<uint8_t>(B * cfg->text_len * D * es);
-  w.vct = bp.take<uint8_t>(B * H * hd * vt_ld(cfg->text_len) * es);
-  w.kci = cfg->img_len ? bp.take<uint8_t>(B * cfg->img_len * D * es) : nullptr;
-  w.vcit = cfg->img_len ? bp.take<uint8_t>(B * H * hd * vt_ld(cfg->img_len) * es) : nullptr;
+  w.kvc = bp.take<uint8_t>(B * cfg->text_len * 2 * D * es);  // rows k | v
+  w.kvci = cfg->img_len ? bp.take<uint8_t>(B * cfg->img_len * 2 * D * es) : nullptr;
   w.h = bp.take<uint8_t>(M * (long long)cfg->ffn * es);
   w.patchA = bp.take<uint8_t>(patch_ws_bytes((int)B, cfg->c_in, cfg->frames, cfg->height, cfg->width, f32));
   w.tsin = bp.take<float>(B * cfg->freq_dim);
@@ -239,7 +234,7 @@ static FwdWs plan_forward(const wan_dit_config* cfg, void* ws) {
   w.e0 = bp.take<float>(B * 6 * D);
   w.hm = bp.take<float>(B * 2 * D);
   w.mods = bp.take<float>((long long)cfg->blocks * B * 6 * D);
-  w.rope = bp.take<float2>(rope_table_entries(cfg->frames, cfg->height / 2, cfg->width / 2, (int)hd));
+  w.rope = bp.take<float>((size_t)hd / 2);
   w.bytes = (size_t)round_up((long long)bp.off, 1024);
   return w;
 }
@@ -310,7 +305,7 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
   const int M = B * L;
 
   // 3D RoPE table and the shared time embedding -> six modulation vectors per block.
-  WAN_TRY(launch_rope_table(c, W.rope, Fg, Hg, Wg, hd, cfg->theta));
+  WAN_TRY(launch_rope_table(c, W.rope, hd, cfg->theta));
   const RopeGeom rg = rope_geom(W.rope, Fg, Hg, Wg, hd);
   WAN_TRY(time_embed_impl(c, cfg, w, t, t_stride, W.tsin, W.h1, W.e, W.e0, W.hm));
   {
@@ -322,34 +317,29 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
   WAN_TRY(patchify_impl(c, latent, lat_bstride, w->patch_w, w->patch_b, W.x, B, cfg->c_in, cfg->frames,
                         cfg->height, cfg->width, D, f32, W.patchA));
 
-  const long long ldvt = vt_ld(L), ldvc = vt_ld(Lt), ldvi = vt_ld(Li > 0 ? Li : 1);
   for (int i = 0; i < cfg->blocks; ++i) {
     const wan_block_weights& bw = w->blocks[i];
     const float* mod = W.mods + (long long)i * B * 6 * D;  // [B][6][D]
 
-    // --- self-attention: y = LN(x)(1+sc1)+sh1; q,k (RoPE), v^T; attention; x += g1 (o Wo^T + bo)
+    // --- self-attention: y = LN(x)(1+sc1)+sh1; q,k (RoPE), v; attention; x += g1 (o Wo^T + bo)
     WAN_TRY(launch_ln_mod(c, W.x, mod + 0 * D, mod + 1 * D, 6LL * D, W.y, f32, M, L, D, cfg->eps));
     {
       EpiParams ep = epi_base(EPI_QKV, M, 3 * D, L, bw.qkv_b, f32);
-      ep.qk = W.qk;
-      ep.ldqk = 2LL * D;
-      ep.qk_type = f32 ? OUT_F32 : OUT_F16;  // q, k feed the QK^T MMA in fp16
-      ep.vt_type = f32 ? OUT_F32 : OUT_BF16;
-      ep.n_qk = 2 * D;
+      ep.out = W.qkv;
+      ep.ldo = 3LL * D;
+      ep.out_type = f32 ? OUT_F32 : OUT_BF16;
       ep.n_rot = 2 * D;
-      ep.vt = W.vt;
-      ep.ld_vt = ldvt;
+      ep.n_f16 = f32 ? 0 : 2 * D;  // q, k feed the QK^T MMA in fp16
       ep.head_dim = hd;
-      ep.heads = H;
       ep.rope = rg;
       WAN_TRY(proj(c, f32, W.y, D, D, bw.qkv_w, D, D, M, 3 * D, D, 0, ep, "gemm_qkv_rope"));
     }
     {
       AttnArgs a;
       memset(&a, 0, sizeof(a));
-      a.q = W.qk; a.ldq = 2LL * D; a.q_row_len = 2 * D; a.q_col = 0;
-      a.k = W.qk; a.ldk = 2LL * D; a.k_row_len = 2 * D; a.k_col = D;
-      a.vt = W.vt; a.ld_vt = ldvt;
+      a.q = W.qkv; a.ldq = 3LL * D; a.q_row_len = 3 * D; a.q_col = 0;
+      a.k = W.qkv; a.ldk = 3LL * D; a.k_row_len = 3 * D; a.k_col = D;
+      a.v = W.qkv; a.ldv = 3LL * D; a.v_row_len = 3 * D; a.v_col = 2 * D;
       a.o = W.o; a.ldo = D; a.o_col = 0;
       a.B = B; a.Lq = L; a.Lkv = L; a.H = H; a.head_dim = hd;
       a.tag = "attn_self";
@@ -376,27 +366,21 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
     }
     for (int seg = 0; seg < (Li ? 2 : 1); ++seg) {
       const int Lk = seg ? Li : Lt;
-      void* kbuf = seg ? W.kci : W.kc;
-      void* vbuf = seg ? W.vcit : W.vct;
-      const long long ldv = seg ? ldvi : ldvc;
+      void* kv = seg ? W.kvci : W.kvc;
       EpiParams ep = epi_base(EPI_QKV, B * Lk, 2 * D, Lk, seg ? bw.ckvi_b : bw.ckv_b, f32);
-      ep.qk = kbuf;
-      ep.ldqk = D;
-      ep.qk_type = f32 ? OUT_F32 : OUT_F16;
-      ep.vt_type = f32 ? OUT_F32 : OUT_BF16;
-      ep.n_qk = D;
+      ep.out = kv;
+      ep.ldo = 2LL * D;
+      ep.out_type = f32 ? OUT_F32 : OUT_BF16;
       ep.n_rot = 0;
-      ep.vt = vbuf;
-      ep.ld_vt = ldv;
+      ep.n_f16 = f32 ? 0 : D;  // k in fp16, v in bf16
       ep.head_dim = hd;
-      ep.heads = H;
       WAN_TRY(proj(c, f32, seg ? ctx_img : ctx_txt, D, D, seg ? bw.ckvi_w : bw.ckv_w, D, D, B * Lk, 2 * D, D, 0, ep,
                    "gemm_cross_kv"));
       AttnArgs a;
       memset(&a, 0, sizeof(a));
       a.q = W.qc; a.ldq = D; a.q_row_len = D; a.q_col = 0;
-      a.k = kbuf; a.ldk = D; a.k_row_len = D; a.k_col = 0;
-      a.vt = vbuf; a.ld_vt = ldv;
+      a.k = kv; a.ldk = 2LL * D; a.k_row_len = 2 * D; a.k_col = 0;
+      a.v = kv; a.ldv = 2LL * D; a.v_row_len = 2 * D; a.v_col = D;
       a.o = W.o; a.ldo = D; a.o_col = 0;
       a.B = B; a.Lq = L; a.Lkv = Lk; a.H = H; a.head_dim = hd;
       a.accumulate = seg;
@@ -489,7 +473,7 @@ int wan_patchify(const float* latent, const void* w, const void* b, float* x, in
   WAN_TRY(check_dtype(dtype));
   if (!latent || !w || !b || !x || B <= 0 || C <= 0 || F <= 0 || H <= 0 || W <= 0 || D <= 0 || H % 2 || W % 2)
     return WAN_ERR_INVALID_ARG;
-  if (D % 32 || !aligned16(latent) || !aligned16(w) || !aligned16(x)) return WAN_ERR_UNSUPPORTED;
+  if (D % 32 || !aligned16(latent) || !aligned16(w) || !aligned16(b) || !aligned16(x)) return WAN_ERR_UNSUPPORTED;
   if (!ws || ws_bytes < patch_ws_bytes(B, C, F, H, W, dtype == WAN_F32) || !aligned16(ws)) return WAN_ERR_WORKSPACE;
   LaunchCtx c;
   WAN_TRY(launch_ctx(stream, &c));
@@ -511,10 +495,9 @@ size_t wan_attn_workspace_size(int B, int L, int H, int d, int dtype) {
   if (B <= 0 || L <= 0 || H <= 0 || d <= 0) return 0;
   const size_t es = dtype == WAN_F32 ? 4 : 2;
   Bump bp(nullptr);
-  bp.take<float2>((size_t)L * d);  // RoPE table (upper bound)
-  bp.take<uint8_t>((size_t)B * L * H * d * es);
-  bp.take<uint8_t>((size_t)B * L * H * d * es);
-  bp.take<uint8_t>((size_t)B * H * d * vt_ld(L) * es);
+  bp.take<float>((size_t)d / 2);   // RoPE pair frequencies
+  bp.take<uint8_t>((size_t)B * L * H * d * es);  // rotated q
+  bp.take<uint8_t>((size_t)B * L * H * d * es);  // rotated k
   return (size_t)round_up((long long)bp.off, 1024);
 }
 
@@ -528,20 +511,20 @@ int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B,
   if (apply_rope && (Fg <= 0 || Hg <= 0 || Wg <= 0 || (long long)Fg * Hg * Wg != L)) return WAN_ERR_INVALID_ARG;
   if ((!f32 && d != 64 && d != 128) || (f32 && (d > 128 || d % 2))) return WAN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return WAN_ERR_UNSUPPORTED;
-  if (!ws || ws_bytes < wan_attn_workspace_size(B, L, H, d, dtype) || (reinterpret_cast<uintptr_t>(ws) & 1023))
+  if (apply_rope && (!ws || ws_bytes < wan_attn_workspace_size(B, L, H, d, dtype) ||
+                     (reinterpret_cast<uintptr_t>(ws) & 1023)))
     return WAN_ERR_WORKSPACE;
   LaunchCtx c;
   WAN_TRY(launch_ctx(stream, &c));
-  const size_t es = f32 ? 4 : 2;
-  Bump bp(ws);
-  float2* tab = bp.take<float2>((size_t)L * d);
-  void* qr = bp.take<uint8_t>((size_t)B * L * H * d * es);
-  void* kr = bp.take<uint8_t>((size_t)B * L * H * d * es);
-  void* vt = bp.take<uint8_t>((size_t)B * H * d * vt_ld(L) * es);
   const void* qa = q;
   const void* ka = k;
   if (apply_rope) {
-    WAN_TRY(launch_rope_table(c, tab, Fg, Hg, Wg, d, theta));
+    const size_t es = f32 ? 4 : 2;
+    Bump bp(ws);
+    float* tab = bp.take<float>((size_t)d / 2);
+    void* qr = bp.take<uint8_t>((size_t)B * L * H * d * es);
+    void* kr = bp.take<uint8_t>((size_t)B * L * H * d * es);
+    WAN_TRY(launch_rope_table(c, tab, d, theta));
     const RopeGeom g = rope_geom(tab, Fg, Hg, Wg, d);
     const int in_type = f32 ? OUT_F32 : (qk_dtype == WAN_F16 ? OUT_F16 : OUT_BF16);
     WAN_TRY(launch_rope_apply(c, q, qr, g, B, L, H, d, in_type));
@@ -549,13 +532,12 @@ int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B,
     qa = qr;
     ka = kr;
   }
-  WAN_TRY(launch_transpose_v(c, v, vt, vt_ld(L), B, L, H, d, f32));
   AttnArgs a;
   memset(&a, 0, sizeof(a));
   const int D = H * d;
   a.q = qa; a.ldq = D; a.q_row_len = D;
   a.k = ka; a.ldk = D; a.k_row_len = D;
-  a.vt = vt; a.ld_vt = vt_ld(L);
+  a.v = v; a.ldv = D; a.v_row_len = D;
   a.o = o; a.ldo = D;
   a.B = B; a.Lq = L; a.Lkv = L; a.H = H; a.head_dim = d;
   a.tag = "attn_self";
@@ -564,17 +546,14 @@ int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B,
 }
 
 size_t wan_cross_attn_workspace_size(int B, int Lt, int Li, int H, int d, int dtype) {
-  if (B <= 0 || Lt <= 0 || Li < 0 || H <= 0 || d <= 0) return 0;
-  const size_t es = dtype == WAN_F32 ? 4 : 2;
-  Bump bp(nullptr);
-  bp.take<uint8_t>((size_t)B * H * d * vt_ld(Lt) * es);
-  if (Li) bp.take<uint8_t>((size_t)B * H * d * vt_ld(Li) * es);
-  return (size_t)round_up((long long)bp.off, 1024);
+  (void)B, (void)Lt, (void)Li, (void)H, (void)d, (void)dtype;
+  return 0;  // the kernels read q, k and v in place
 }
 
 int wan_cross_attn(const void* q, const void* kt, const void* vt, const void* ki, const void* vi, void* o, int B,
                    int L, int Lt, int Li, int H, int d, int dtype, int qk_dtype, void* ws, size_t ws_bytes,
                    wan_stream_t stream) {
+  (void)ws, (void)ws_bytes;
   WAN_TRY(check_dtype(dtype));
   WAN_TRY(check_qk_dtype(dtype, qk_dtype));
   const int f32 = dtype == WAN_F32;
@@ -583,25 +562,16 @@ int wan_cross_attn(const void* q, const void* kt, const void* vt, const void* ki
   if ((!f32 && d != 64 && d != 128) || (f32 && (d > 128 || d % 2))) return WAN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(kt) || !aligned16(vt) || !aligned16(o) || (Li && (!aligned16(ki) || !aligned16(vi))))
     return WAN_ERR_UNSUPPORTED;
-  if (!ws || ws_bytes < wan_cross_attn_workspace_size(B, Lt, Li, H, d, dtype) ||
-      (reinterpret_cast<uintptr_t>(ws) & 1023))
-    return WAN_ERR_WORKSPACE;
   LaunchCtx c;
   WAN_TRY(launch_ctx(stream, &c));
-  const size_t es = f32 ? 4 : 2;
-  Bump bp(ws);
-  void* vtt = bp.take<uint8_t>((size_t)B * H * d * vt_ld(Lt) * es);
-  void* vit = Li ? bp.take<uint8_t>((size_t)B * H * d * vt_ld(Li) * es) : nullptr;
   const int D = H * d;
   for (int seg = 0; seg < (Li ? 2 : 1); ++seg) {
     const int Lk = seg ? Li : Lt;
-    void* vtr = seg ? vit : vtt;
-    WAN_TRY(launch_transpose_v(c, seg ? vi : vt, vtr, vt_ld(Lk), B, Lk, H, d, f32));
     AttnArgs a;
     memset(&a, 0, sizeof(a));
     a.q = q; a.ldq = D; a.q_row_len = D;
     a.k = seg ? ki : kt; a.ldk = D; a.k_row_len = D;
-    a.vt = vtr; a.ld_vt = vt_ld(Lk);
+    a.v = seg ? vi : vt; a.ldv = D; a.v_row_len = D;
     a.o = o; a.ldo = D;
     a.B = B; a.Lq = L; a.Lkv = Lk; a.H = H; a.head_dim = d;
     a.accumulate = seg;
@@ -618,7 +588,7 @@ int wan_ffn(const void* y, const void* w1, const void* b1, const void* w2, const
   const int f32 = dtype == WAN_F32;
   if (!y || !w1 || !w2 || !x_inout || !h_ws || B <= 0 || L <= 0 || D <= 0 || F <= 0) return WAN_ERR_INVALID_ARG;
   if (D % 32 || F % 32 || !aligned16(y) || !aligned16(w1) || !aligned16(w2) || !aligned16(x_inout) ||
-      !aligned16(h_ws) || (gate && !aligned16(gate)))
+      !aligned16(h_ws) || (gate && !aligned16(gate)) || (b1 && !aligned16(b1)) || (b2 && !aligned16(b2)))
     return WAN_ERR_UNSUPPORTED;
   LaunchCtx c;
   WAN_TRY(launch_ctx(stream, &c));
@@ -646,7 +616,8 @@ int wan_linear(const void* x, const void* w, const void* b, void* out, int M, in
   if (gate && rows_per_gate <= 0) return WAN_ERR_INVALID_ARG;
   if (f32 && out_dtype != WAN_F32) return WAN_ERR_UNSUPPORTED;
   if (epilogue == WAN_EPI_RESIDUAL && out_dtype != WAN_F32) return WAN_ERR_UNSUPPORTED;
-  if (N % 32 || K % 8 || !aligned16(x) || !aligned16(w) || !aligned16(out) || (gate && !aligned16(gate)))
+  if (N % 32 || K % 8 || !aligned16(x) || !aligned16(w) || !aligned16(out) || (gate && !aligned16(gate)) ||
+      (b && !aligned16(b)))
     return WAN_ERR_UNSUPPORTED;
   LaunchCtx c;
   WAN_TRY(launch_ctx(stream, &c));
@@ -675,7 +646,8 @@ int wan_text_embed(const void* text, const void* w1, const void* b1, const void*
   WAN_TRY(check_dtype(dtype));
   const int f32 = dtype == WAN_F32;
   if (!text || !w1 || !w2 || !ctx || B <= 0 || Lt <= 0 || Ct <= 0 || D <= 0) return WAN_ERR_INVALID_ARG;
-  if (D % 32 || Ct % 8 || !aligned16(text) || !aligned16(w1) || !aligned16(w2) || !aligned16(ctx))
+  if (D % 32 || Ct % 8 || !aligned16(text) || !aligned16(w1) || !aligned16(w2) || !aligned16(ctx) ||
+      (b1 && !aligned16(b1)) || (b2 && !aligned16(b2)))
     return WAN_ERR_UNSUPPORTED;
   if (!ws || ws_bytes < wan_text_embed_workspace_size(B, Lt, D, dtype) || !aligned16(ws)) return WAN_ERR_WORKSPACE;
   LaunchCtx c;

@@ -6,9 +6,9 @@
 // sequence in 128-key tiles.  Tensor memory holds, per query tile, the score tile S
 // (128 fp32 columns; the bf16 probabilities P overwrite its first 64 columns) and the
 // output accumulator O (d fp32 columns): 2 x 256 = 512 columns.
-//   warp 0      TMA: Q once, then K and V^T tiles into 2-deep rings
+//   warp 0      TMA: Q once, then K and V tiles into 2-deep rings
 //   warp 1      tcgen05.mma from one thread: S_i = Q_i K^T (both operands in smem),
-//               O_i += P_i V (P from TMEM, V^T tile from smem), ping-ponging the tiles
+//               O_i += P_i V (P from TMEM, V tile from smem), ping-ponging the tiles
 //   warps 4..11 softmax, one warpgroup per query tile, one thread per query row: fp32
 //               running max and sum, exp2 on the MUFU unit, lazy rescale of O in TMEM
 //               only when the running max grows by more than 2^8, final 1/l and store.
@@ -17,7 +17,9 @@
 // Per score element the softmax issues half an FFMA2 (scale and max subtraction on
 // packed pairs), one MUFU ex2, half a bf16x2 pack, half an FADD2 (row sum) and half a
 // 3-input max; the ragged-tile mask runs only on the last key tile.
-// V arrives transposed ([d, keys], keys contiguous) so every MMA operand is K-major.
+// V is read in its natural [token, H*d] layout: in the PV product it is the B operand
+// with N = d contiguous, i.e. MN-major (descriptor LBO = the 64-column box stride,
+// SBO = 1024 bytes per 8 keys), so no transposed copy of V is ever written.
 // Ragged tails: keys past Lkv are zero-filled by TMA and masked to -inf; query rows
 // past Lq are computed on zero rows and not stored.
 #include <type_traits>
@@ -33,9 +35,9 @@ struct AttnCfg {
   static constexpr int BKV = 128;
   static constexpr int Q_BYTES = BQ * HD * 2;    // HD/64 boxes of 128 rows x 128 B
   static constexpr int K_BYTES = BKV * HD * 2;   // HD/64 boxes of 128 rows x 128 B
-  static constexpr int V_BYTES = HD * BKV * 2;   // 2 boxes of HD rows x 128 B (64 keys)
+  static constexpr int V_BYTES = BKV * HD * 2;   // HD/64 boxes of 128 keys x 128 B
   static constexpr int Q_BOX = BQ * 128;         // bytes per 64-column box of a Q/K tile
-  static constexpr int V_BOX = HD * 128;         // bytes per 64-key box of a V^T tile
+  static constexpr int V_BOX = BKV * 128;        // bytes per 64-column box of a V tile
   static constexpr int SMEM_TILES = 2 * Q_BYTES + 2 * K_BYTES + 2 * V_BYTES;
   static constexpr int SMEM = SMEM_TILES + 256 + 1024;
   static constexpr int TMEM_COLS = 512;
@@ -49,7 +51,7 @@ struct AttnCfg {
 
 struct AttnParams {
   int Lq, Lkv, H;
-  int q_col, k_col;       // column offset of head 0 inside the q / k rows
+  int q_col, k_col, v_col;  // column offset of head 0 inside the q / k / v rows
   int nq_pairs;           // ceil(ceil(Lq/128)/2)
   float scale_log2;       // log2(e) / sqrt(d)
   bf16* o;                // [B, Lq, ldo]
@@ -136,8 +138,9 @@ __global__ void __launch_bounds__(384, 1)
       kissued = j + 1;
       if (!mbar_wait(&v_empty[s], ph ^ 1, status, kDevTimeoutAttn)) { ok = false; break; }
       mbar_arrive_expect_tx(&v_full[s], Cfg::V_BYTES);
-      for (int c = 0; c < 2; ++c)
-        tma_load_2d(sV + s * Cfg::V_BYTES + c * Cfg::V_BOX, &tmV, &v_full[s], j * Cfg::BKV + c * 64, bh * HD);
+      for (int c = 0; c < HD / 64; ++c)
+        tma_load_3d(sV + s * Cfg::V_BYTES + c * Cfg::V_BOX, &tmV, &v_full[s], p.v_col + h * HD + c * 64,
+                    j * Cfg::BKV, b);
       vissued = j + 1;
     }
     if (!ok) {  // error path: let issued copies land
@@ -151,13 +154,14 @@ __global__ void __launch_bounds__(384, 1)
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
     constexpr uint32_t idS = QK_F16 ? make_idesc_f16(128, Cfg::BKV) : make_idesc_bf16(128, Cfg::BKV);
-    constexpr uint32_t idO = make_idesc_bf16(128, HD);
+    constexpr uint32_t idO = make_idesc_bf16(128, HD) | kIdescBMnMajor;
     bool ok = mbar_wait(q_full, 0, status, kDevTimeoutAttn) && mbar_wait(&k_full[0], 0, status, kDevTimeoutAttn);
     // Descriptor low words of every operand buffer, computed once: the issuing thread
     // shares its SM sub-partition with two softmax warps, so each MMA costs only an add.
     const uint32_t q_lo0 = sdesc_sw128_lo(smem_u32(sQ)), q_lo1 = sdesc_sw128_lo(smem_u32(sQ + Cfg::Q_BYTES));
     const uint32_t k_lo0 = sdesc_sw128_lo(smem_u32(sK)), k_lo1 = sdesc_sw128_lo(smem_u32(sK + Cfg::K_BYTES));
-    const uint32_t v_lo0 = sdesc_sw128_lo(smem_u32(sV)), v_lo1 = sdesc_sw128_lo(smem_u32(sV + Cfg::V_BYTES));
+    const uint32_t v_lo0 = sdesc_sw128_mn_lo(smem_u32(sV), Cfg::V_BOX);
+    const uint32_t v_lo1 = sdesc_sw128_mn_lo(smem_u32(sV + Cfg::V_BYTES), Cfg::V_BOX);
     auto issue_S = [&](int i, int ks) {
       const uint32_t qa = i ? q_lo1 : q_lo0;
       const uint32_t ka = ks ? k_lo1 : k_lo0;
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t pa = tmem_base + i * 256;
 #pragma unroll
       for (int kk = 0; kk < Cfg::BKV / 16; ++kk) {
-        const uint32_t off = ((kk >> 2) * Cfg::V_BOX + (kk & 3) * 32) >> 4;
+        const uint32_t off = (kk * 16 * 128) >> 4;  // 16 keys = 16 rows of 128 bytes
         tc_mma_ts_lo(d, pa + kk * 8, va + off, idO, (acc | (uint32_t)kk) != 0 ? 1u : 0u);
       }
     };
@@ -404,8 +408,8 @@ int attention_bf16(const LaunchCtx& c, const AttnArgs& a) {
   st = make_tmap_3d(&tk, a.k, qkt, 2, (uint64_t)a.k_row_len, (uint64_t)a.Lkv,
                     (uint64_t)a.B, (uint64_t)a.ldk * 2, (uint64_t)a.ldk * 2 * a.Lkv, 64, 128);
   if (st != WAN_OK) return st;
-  st = make_tmap_2d(&tv, a.vt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.Lkv,
-                    (uint64_t)a.B * a.H * HD, (uint64_t)a.ld_vt * 2, 64, (uint32_t)HD);
+  st = make_tmap_3d(&tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.v_row_len, (uint64_t)a.Lkv,
+                    (uint64_t)a.B, (uint64_t)a.ldv * 2, (uint64_t)a.ldv * 2 * a.Lkv, 64, 128);
   if (st != WAN_OK) return st;
   AttnParams p;
   p.Lq = a.Lq;
@@ -413,6 +417,7 @@ int attention_bf16(const LaunchCtx& c, const AttnArgs& a) {
   p.H = a.H;
   p.q_col = a.q_col;
   p.k_col = a.k_col;
+  p.v_col = a.v_col;
   p.nq_pairs = ((a.Lq + 127) / 128 + 1) / 2;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   p.o = static_cast<bf16*>(a.o);

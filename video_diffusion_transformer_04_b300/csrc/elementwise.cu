@@ -212,26 +212,28 @@ int launch_patch_gather(const LaunchCtx& c, const float* latent, long long laten
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
 
-// ------------------------------------------------------------------ RoPE table
-// (cos, sin) of pos * theta^(-2j/d_a) for every axis a, grid position and pair j,
-// evaluated in double precision.
-__global__ void rope_table_kernel(float2* tab, RopeGeom g, float theta) {
-  const int total = g.Fg * g.nf + g.Hg * g.nh + g.Wg * g.nw;
-  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
-    int r = e, pairs, pos, j;
-    if (r < g.Fg * g.nf) { pairs = g.nf; pos = r / pairs; j = r % pairs; }
-    else if ((r -= g.Fg * g.nf) < g.Hg * g.nh) { pairs = g.nh; pos = r / pairs; j = r % pairs; }
-    else { r -= g.Hg * g.nh; pairs = g.nw; pos = r / pairs; j = r % pairs; }
-    const double ang = (double)pos * pow((double)theta, -2.0 * j / (2.0 * pairs));
-    tab[e] = make_float2((float)cos(ang), (float)sin(ang));
+// ------------------------------------------------------------------ RoPE frequencies
+// omega of pair j of axis a (n_a = d_a / 2 pairs): theta^(-2j/d_a), in double precision.
+__global__ void rope_table_kernel(float* omega, RopeGeom g, float theta) {
+  const int total = g.nf + g.nh + g.nw;
+  for (int e = threadIdx.x; e < total; e += blockDim.x) {
+    int j = e, pairs = g.nf;
+    if (j >= g.nf) {
+      j -= g.nf;
+      pairs = g.nh;
+      if (j >= g.nh) {
+        j -= g.nh;
+        pairs = g.nw;
+      }
+    }
+    omega[e] = (float)pow((double)theta, -2.0 * j / (2.0 * pairs));
   }
 }
 
-int launch_rope_table(const LaunchCtx& c, float2* tab, int Fg, int Hg, int Wg, int head_dim, float theta) {
-  RopeGeom g = rope_geom(tab, Fg, Hg, Wg, head_dim);
-  const int total = Fg * g.nf + Hg * g.nh + Wg * g.nw;
+int launch_rope_table(const LaunchCtx& c, float* omega, int head_dim, float theta) {
+  RopeGeom g = rope_geom(omega, 1, 1, 1, head_dim);
   count_launch("rope_table", c.stream, true);
-  rope_table_kernel<<<(total + 255) / 256, 256, 0, c.stream>>>(tab, g, theta);
+  rope_table_kernel<<<1, 128, 0, c.stream>>>(omega, g, theta);
   count_launch("rope_table", c.stream, false);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
@@ -328,39 +330,6 @@ int launch_block_mods(const LaunchCtx& c, const float* e0, const void* const* mo
 }
 
 // ------------------------------------------------------------------ layout helpers
-template <typename T>
-__global__ void transpose_v_kernel(const T* __restrict__ v, T* __restrict__ vt, long long ld_vt, int L, int H, int d) {
-  __shared__ T tile[32][33];
-  const int bh = blockIdx.z;
-  const int b = bh / H, h = bh - (bh / H) * H;
-  const int l0 = blockIdx.x * 32, d0 = blockIdx.y * 32;
-  const long long D = (long long)H * d;
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    const int l = l0 + r, dd = d0 + threadIdx.x;
-    if (l < L && dd < d) tile[r][threadIdx.x] = v[((long long)b * L + l) * D + h * d + dd];
-  }
-  __syncthreads();
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    const int dd = d0 + r, l = l0 + threadIdx.x;
-    if (l < L && dd < d) vt[((long long)bh * d + dd) * ld_vt + l] = tile[threadIdx.x][r];
-  }
-}
-
-int launch_transpose_v(const LaunchCtx& c, const void* v, void* vt, long long ld_vt, int B, int L, int H, int d,
-                       int f32) {
-  if (B * L <= 0) return WAN_OK;
-  dim3 grid((L + 31) / 32, (d + 31) / 32, B * H), block(32, 8);
-  count_launch("transpose_v", c.stream, true);
-  if (f32)
-    transpose_v_kernel<float><<<grid, block, 0, c.stream>>>(static_cast<const float*>(v), static_cast<float*>(vt),
-                                                            ld_vt, L, H, d);
-  else
-    transpose_v_kernel<bf16><<<grid, block, 0, c.stream>>>(static_cast<const bf16*>(v), static_cast<bf16*>(vt), ld_vt,
-                                                           L, H, d);
-  count_launch("transpose_v", c.stream, false);
-  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
-}
-
 template <typename Tin, typename Tout>
 __global__ void rope_apply_kernel(const Tin* __restrict__ in, Tout* __restrict__ out, RopeGeom g, long long rows,
                                   int L, int H, int d) {

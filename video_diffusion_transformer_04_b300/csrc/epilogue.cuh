@@ -14,14 +14,14 @@ enum EpiKind : int {
   EPI_STORE = 0,  // out[m, n] = acc + bias
   EPI_GELU = 1,   // out[m, n] = GELU(acc + bias)
   EPI_RESID = 2,  // resid[m, n] += gate[b, n] * (acc + bias)   (gate NULL: 1)
-  EPI_QKV = 3,    // cols [0, n_qk): (RoPE on [0, n_rot)) -> qk[m, n]; cols [n_qk, N): -> vt
+  EPI_QKV = 3,    // out[m, n] = acc + bias, RoPE on cols [0, n_rot), fp16 on cols [0, n_f16)
   EPI_HEAD = 4,   // depatchify: vout[b, c, f, 2i+di, 2j+dj] = acc + bias, n = c*4 + di*2 + dj
 };
 
 struct RopeGeom {
-  const float2* tab;  // [Fg*nf | Hg*nh | Wg*nw] (cos, sin)
-  int Fg, Hg, Wg;     // token grid
-  int nf, nh, nw;     // rotation pairs per axis
+  const float* omega;  // [nf | nh | nw] angular frequency of each rotation pair of a head
+  int Fg, Hg, Wg;      // token grid
+  int nf, nh, nw;      // rotation pairs per axis
 };
 
 // Storage types of epilogue outputs.
@@ -42,24 +42,55 @@ struct EpiParams {
   long long ldr;
   const float* gate;
   long long ld_gate;  // gate batch stride (elements)
-  // EPI_QKV
-  void* qk;
-  long long ldqk;
-  int qk_type;  // OutType of q|k
-  int vt_type;  // OutType of v^T (OUT_BF16 or OUT_F32)
-  int n_qk, n_rot;
-  void* vt;            // [(b*H + h)*hd + dd] rows of ld_vt elements
-  long long ld_vt;
-  int head_dim, heads;
+  // EPI_QKV (also uses out / ldo / out_type for the columns past n_f16)
+  int n_rot, n_f16;
+  int head_dim;
   RopeGeom rope;
   // EPI_HEAD
   float* vout;
   int C, F, H, W;
 };
 
-__device__ __forceinline__ float epi_bias(const EpiParams& p, int n) {
-  if (p.bias_f32) return static_cast<const float*>(p.bias)[n];
-  return bf2f(static_cast<const bf16*>(p.bias)[n]);
+// v[i] += bias[n0 + i] with 16-byte vector loads (bias rows are 16-byte aligned and n0
+// is a multiple of CNT).
+template <int CNT>
+__device__ __forceinline__ void epi_add_bias(const EpiParams& p, int n0, float* v) {
+  if (!p.bias) return;
+  if (p.bias_f32) {
+    const float4* b = reinterpret_cast<const float4*>(static_cast<const float*>(p.bias) + n0);
+#pragma unroll
+    for (int i = 0; i < CNT / 4; ++i) {
+      const float4 q = b[i];
+      v[4 * i] += q.x;
+      v[4 * i + 1] += q.y;
+      v[4 * i + 2] += q.z;
+      v[4 * i + 3] += q.w;
+    }
+  } else if constexpr (CNT % 8 == 0) {
+    const uint4* b = reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.bias) + n0);
+#pragma unroll
+    for (int i = 0; i < CNT / 8; ++i) {
+      const uint4 q = b[i];
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 f = unpack_bf16x2(w[u]);
+        v[8 * i + 2 * u] += f.x;
+        v[8 * i + 2 * u + 1] += f.y;
+      }
+    }
+  } else {
+    const uint2* b = reinterpret_cast<const uint2*>(static_cast<const bf16*>(p.bias) + n0);
+#pragma unroll
+    for (int i = 0; i < CNT / 4; ++i) {
+      const uint2 q = b[i];
+      const float2 lo = unpack_bf16x2(q.x), hi = unpack_bf16x2(q.y);
+      v[4 * i] += lo.x;
+      v[4 * i + 1] += lo.y;
+      v[4 * i + 2] += hi.x;
+      v[4 * i + 3] += hi.y;
+    }
+  }
 }
 
 // Store CNT consecutive values (CNT % 4 == 0, 16-byte aligned destinations for CNT >= 8).
@@ -100,25 +131,25 @@ __device__ __forceinline__ void epi_store_row(void* base, int type, long long of
 }
 
 // Rotate the adjacent pairs of v (CNT values starting at head-dim index dd0, even) by
-// the 3D-RoPE angles of token l.
+// the 3D-RoPE angles of token l: pair j of the head turns by pos_a(j) * omega[j], pos_a
+// the token's frame, height or width index for the axis that owns pair j.  The sine and
+// cosine come from the SFU (__sincosf, absolute error about 1e-6 at the grid's angles).
 template <int CNT>
 __device__ __forceinline__ void epi_rope(const RopeGeom& g, int head_dim, int dd0, int l, float* v) {
-  const int pf = l / (g.Hg * g.Wg);
-  const int ph = (l / g.Wg) % g.Hg;
-  const int pw = l % g.Wg;
-  const float2* tf = g.tab + pf * g.nf;
-  const float2* th = g.tab + g.Fg * g.nf + ph * g.nh;
-  const float2* tw = g.tab + g.Fg * g.nf + g.Hg * g.nh + pw * g.nw;
+  const int hw = g.Hg * g.Wg;
+  const int pf = l / hw;
+  const int rem = l - pf * hw;
+  const int ph = rem / g.Wg;
+  const int pw = rem - ph * g.Wg;
 #pragma unroll
   for (int i = 0; i < CNT / 2; ++i) {
     const int pair = (dd0 >> 1) + i;  // pair index within the head
-    float2 cs;
-    if (pair < g.nf) cs = tf[pair];
-    else if (pair < g.nf + g.nh) cs = th[pair - g.nf];
-    else cs = tw[pair - g.nf - g.nh];
+    const int pos = pair < g.nf ? pf : (pair < g.nf + g.nh ? ph : pw);
+    float sn, cs;
+    __sincosf((float)pos * g.omega[pair], &sn, &cs);
     const float x0 = v[2 * i], x1 = v[2 * i + 1];
-    v[2 * i] = x0 * cs.x - x1 * cs.y;
-    v[2 * i + 1] = x0 * cs.y + x1 * cs.x;
+    v[2 * i] = x0 * cs - x1 * sn;
+    v[2 * i + 1] = x0 * sn + x1 * cs;
   }
   (void)head_dim;
 }
@@ -132,10 +163,7 @@ __device__ __forceinline__ void epi_resid_values(const EpiParams& p, int m, int 
     for (int i = 0; i < CNT; ++i) v[i] = 0.f;
     return;
   }
-  if (p.bias) {
-#pragma unroll
-    for (int i = 0; i < CNT; ++i) v[i] += epi_bias(p, n0 + i);
-  }
+  epi_add_bias<CNT>(p, n0, v);
   if (p.gate) {
     const float* g = p.gate + (long long)(m / p.rows_per_batch) * p.ld_gate + n0;
 #pragma unroll
@@ -153,10 +181,7 @@ __device__ __forceinline__ void epi_resid_values(const EpiParams& p, int m, int 
 // n0 % CNT == 0 and the chunk never straddles a section or head boundary).
 template <int CNT>
 __device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int m, int n0, float* v) {
-  if (p.bias) {
-#pragma unroll
-    for (int i = 0; i < CNT; ++i) v[i] += epi_bias(p, n0 + i);
-  }
+  epi_add_bias<CNT>(p, n0, v);
   const int b = m / p.rows_per_batch;
   const int l = m - b * p.rows_per_batch;
   switch (p.kind) {
@@ -183,24 +208,10 @@ __device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int m, int n0
       break;
     }
     case EPI_QKV: {
-      if (n0 < p.n_qk) {
-        if (n0 < p.n_rot) epi_rope<CNT>(p.rope, p.head_dim, n0 % p.head_dim, l, v);
-        epi_store_row<CNT>(p.qk, p.qk_type, (long long)m * p.ldqk + n0, v);
-      } else {
-        const int c = n0 - p.n_qk;
-        const int h = c / p.head_dim;
-        const int dd0 = c - h * p.head_dim;
-        const long long row0 = ((long long)b * p.heads + h) * p.head_dim + dd0;
-        if (p.vt_type == OUT_F32) {
-          float* vt = static_cast<float*>(p.vt);
-#pragma unroll
-          for (int i = 0; i < CNT; ++i) vt[(row0 + i) * p.ld_vt + l] = v[i];
-        } else {
-          bf16* vt = static_cast<bf16*>(p.vt);
-#pragma unroll
-          for (int i = 0; i < CNT; ++i) vt[(row0 + i) * p.ld_vt + l] = __float2bfloat16_rn(v[i]);
-        }
-      }
+      // q | k | v row of the projection: RoPE on q and k, q and k in fp16 for the QK^T
+      // product, v in the call's storage type, all stored in place in one row buffer.
+      if (n0 < p.n_rot) epi_rope<CNT>(p.rope, p.head_dim, n0 % p.head_dim, l, v);
+      epi_store_row<CNT>(p.out, n0 < p.n_f16 ? OUT_F16 : p.out_type, (long long)m * p.ldo + n0, v);
       break;
     }
     case EPI_HEAD: {

@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc = make_idesc_bf16(Cfg::BM, BN);
+    const uint32_t smem_lo0 = sdesc_sw128_lo(smem_u32(smem));
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -127,13 +128,13 @@ __global__ void __launch_bounds__(192, 1)
       for (int kb = 0; kb < num_k; ++kb) {
         if (!mbar_wait(&full[stage], phase, status, kDevTimeoutGemm)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + stage * Cfg::STAGE_BYTES);
-        const uint64_t adesc = make_sdesc_sw128(sa);
-        const uint64_t bdesc = make_sdesc_sw128(sa + Cfg::A_BYTES);
+        // Descriptor low words only (the issuing thread shares its SM sub-partition with
+        // an epilogue warp): stage base + 32 bytes (>> 4 = 2) per K step of 16.
+        const uint32_t a_lo = smem_lo0 + (uint32_t)stage * (Cfg::STAGE_BYTES >> 4);
+        const uint32_t b_lo = a_lo + (Cfg::A_BYTES >> 4);
 #pragma unroll
         for (int kk = 0; kk < Cfg::BK / 16; ++kk)
-          tc_mma_ss(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
-                    (kb | kk) != 0 ? 1u : 0u);
+          tc_mma_ss_lo(d_tmem, a_lo + kk * 2, b_lo + kk * 2, idesc, (kb | kk) != 0 ? 1u : 0u);
         tc_commit(&empty[stage]);
         if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1; }
       }

@@ -34,14 +34,16 @@ struct AttnArgs {
   long long ldk;
   int k_row_len;
   int k_col;
-  const void* vt;  // V transposed: row (b*H + h)*d + dd, column = key
-  long long ld_vt;
+  const void* v;   // [B, Lkv, ldv] rows; head h at columns v_col + h*d
+  long long ldv;
+  int v_row_len;
+  int v_col;
   void* o;
   long long ldo;
   int o_col;
   int B, Lq, Lkv, H, head_dim;
   int accumulate;  // o += result
-  int qk_f16;      // bf16 path: q and k are fp16 (else bf16); v^T and o are bf16
+  int qk_f16;      // bf16 path: q and k are fp16 (else bf16); v and o are bf16
   const char* tag; // profiler label of the launch
 };
 int attention_bf16(const LaunchCtx& c, const AttnArgs& a);
@@ -54,7 +56,8 @@ int launch_cfg_euler(const LaunchCtx& c, float* x, const void* vc, const void* v
                      const float* t_pair, int v_f32);
 int launch_patch_gather(const LaunchCtx& c, const float* latent, long long latent_bstride, void* A, int out_f32,
                         int B, int C, int F, int H, int W, int kpad);
-int launch_rope_table(const LaunchCtx& c, float2* tab, int Fg, int Hg, int Wg, int head_dim, float theta);
+// omega[j] = theta^(-2 j_a / d_a) for the head's d/2 rotation pairs (axis parts f | h | w).
+int launch_rope_table(const LaunchCtx& c, float* omega, int head_dim, float theta);
 // t[b * t_stride] (t_stride 0: one timestep shared by the batch).
 int launch_sinusoid(const LaunchCtx& c, const float* t, int t_stride, float* s, int B, int dim);
 // out[b, n] = act_out(sum_k W[n, k] * act_in(x[b, k]) + bias[n]); act: 0 none, 1 SiLU.
@@ -63,9 +66,6 @@ int launch_small_linear(const LaunchCtx& c, const float* x, const void* W, const
 // mods[blk][b][k][n] = e0[b][k*D + n] + mod_blk[k][n] for `nblk` blocks.
 int launch_block_mods(const LaunchCtx& c, const float* e0, const void* const* mod_ptrs, int nblk, int w_f32,
                       float* mods, int B, int D);
-// v [B, L, H*d] -> vt[(b*H + h)*d + dd][l] (row stride ld_vt), dtype preserved.
-int launch_transpose_v(const LaunchCtx& c, const void* v, void* vt, long long ld_vt, int B, int L, int H, int d,
-                       int f32);
 // Rotate q [B, L, H*d] into out (same layout) with the 3D-RoPE table.  in_type (OutType):
 // bf16 or fp16 input is written out in fp16, fp32 stays fp32.
 int launch_rope_apply(const LaunchCtx& c, const void* in, void* out, const RopeGeom& g, int B, int L, int H, int d,
@@ -73,11 +73,11 @@ int launch_rope_apply(const LaunchCtx& c, const void* in, void* out, const RopeG
 int launch_schedule(const LaunchCtx& c, float* ts, int steps);
 
 // RoPE table geometry for head_dim d on grid (Fg, Hg, Wg).
-inline RopeGeom rope_geom(const float2* tab, int Fg, int Hg, int Wg, int d) {
+inline RopeGeom rope_geom(const float* omega, int Fg, int Hg, int Wg, int d) {
   RopeGeom g;
   const int dh = 2 * (d / 6);
   const int df = d - 2 * dh;
-  g.tab = tab;
+  g.omega = omega;
   g.Fg = Fg;
   g.Hg = Hg;
   g.Wg = Wg;
@@ -85,10 +85,6 @@ inline RopeGeom rope_geom(const float2* tab, int Fg, int Hg, int Wg, int d) {
   g.nh = dh / 2;
   g.nw = dh / 2;
   return g;
-}
-inline size_t rope_table_entries(int Fg, int Hg, int Wg, int d) {
-  RopeGeom g = rope_geom(nullptr, Fg, Hg, Wg, d);
-  return (size_t)Fg * g.nf + (size_t)Hg * g.nh + (size_t)Wg * g.nw;
 }
 
 }  // namespace wan

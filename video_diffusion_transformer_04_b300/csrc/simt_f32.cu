@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(256) attn_f32_kernel(const AttnArgs a, float s
   const int hd = a.head_dim;
   const float* q = static_cast<const float*>(a.q);
   const float* k = static_cast<const float*>(a.k);
-  const float* vt = static_cast<const float*>(a.vt);
+  const float* vv = static_cast<const float*>(a.v);
   if (row < a.Lq)
     for (int d = lane; d < hd; d += 32) sq[warp][d] = q[((long long)b * a.Lq + row) * a.ldq + a.q_col + h * hd + d];
   __syncwarp();
@@ -84,8 +84,8 @@ __global__ void __launch_bounds__(256) attn_f32_kernel(const AttnArgs a, float s
     const float corr = expf(m - mn);
     const float pj = expf(s - mn);
     l = l * corr + pj;
-    const float* vc = vt + (long long)bh * hd * a.ld_vt + j;
-    for (int d = 0; d < hd; ++d) acc[d] = fmaf(pj, vc[(long long)d * a.ld_vt], acc[d] * corr);
+    const float* vr = vv + ((long long)b * a.Lkv + j) * a.ldv + a.v_col + h * hd;
+    for (int d = 0; d < hd; ++d) acc[d] = fmaf(pj, vr[d], acc[d] * corr);
     m = mn;
   }
   float M = m;

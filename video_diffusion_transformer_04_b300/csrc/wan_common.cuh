@@ -212,6 +212,8 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N) {
 __host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// Bit 16 of the instruction descriptor: B is MN-major (N contiguous in shared memory).
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
 
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA with
 // 128-byte swizzle: rows of 128 B (64 bf16 along K), 8-row swizzle atoms of 1024 B.
@@ -233,6 +235,12 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr) {
 // >> 4 to it (the 14-bit start field cannot carry: shared memory is below 256 KB).
 constexpr uint32_t kSdescSw128Hi = (1024u >> 4) | (1u << 14) | (2u << 29);
 __device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr) { return ((saddr & 0x3FFFFu) >> 4) | (1u << 16); }
+// Low word of an MN-major operand descriptor (128-byte swizzle): 64 elements contiguous
+// along M/N per 128-byte row, one row per K index, 8-row groups 1024 bytes apart (SBO, in
+// the common high word) and successive 64-element M/N blocks lbo_bytes apart (LBO).
+__device__ __forceinline__ uint32_t sdesc_sw128_mn_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr & 0x3FFFFu) >> 4) | ((lbo_bytes >> 4) << 16);
+}
 // tcgen05.mma kind::f16 with both operands in shared memory, descriptors given by their
 // low words (high word kSdescSw128Hi).
 __device__ __forceinline__ void tc_mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
