@@ -127,7 +127,7 @@ def blas_threads() -> int:
     return len(os.sched_getaffinity(0))
 
 
-def oracle_step_estimate(s, seed=0, rows_small=16, rows_large=48):
+def oracle_step_estimate(s, seed=0, rows_small=128, rows_large=1024):
     """Time the fp64 oracle on a bounded sample of one block and extrapolate to a step.
 
     Sample: one 1.3B-shaped block on batch entry 0 with every key/value row (LN, QKV over
@@ -313,22 +313,25 @@ def run_ours(a, s):
 
 
 def traffic_record(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if it still matches the source."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/<kernel>_traffic.txt), or None when the kernel source changed since the
+    counters were taken (the summary records the source's sha256 prefix)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
     if not os.path.exists(path):
         return None
     try:
         import hashlib
-        with open(path) as f:
-            rec = json.load(f).get(kernel)
-        if not rec:
-            return None
+        rec = {}
+        for line in open(path):
+            if line.startswith("#") or ":" not in line:
+                continue
+            k, v = line.split(":", 1)
+            rec[k.strip()] = v.strip()
         src = os.path.join(ROOT, "video_diffusion_transformer_04_b300", "csrc", rec["source"])
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if h != rec["source_sha256_16"]:
+        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != rec["source_sha256_16"]:
             return None
-        return rec["dram_bytes_per_launch"]
-    except Exception:
+        return int(rec["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
         return None
 
 
@@ -341,7 +344,7 @@ def run_reference(a, s):
     est = []
     threads, sample = 1, ""
     for i in range(a.warmup + a.steps):
-        step_s, threads, sample, _ = oracle_step_estimate(s, rows_small=8, rows_large=24)
+        step_s, threads, sample, _ = oracle_step_estimate(s, rows_small=16, rows_large=64)
         if i >= a.warmup:
             est.append(step_s)
     step_s = statistics.mean(est)
