@@ -6,8 +6,9 @@
 //   warp 0      TMA producer: A and B tiles (128-byte swizzle) into a STAGES-deep ring
 //   warp 1      allocates TMEM, issues tcgen05.mma (M=128, N=BN, K=16) from one thread,
 //               commits each consumed stage back to the producer
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane = one output
-//               row per thread), bias/GELU/RoPE/gated residual/layout, global stores
+//   warps 2..9  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane = one output
+//               row per thread; two warps per TMEM lane quadrant, each taking half of the
+//               tile's columns), bias/GELU/RoPE/gated residual/layout, global stores
 // The accumulator is double-buffered in TMEM (2 x BN columns), so the epilogue of tile
 // i overlaps the main loop of tile i+1.
 // The gated residual x += gate * (acc + bias) never reads x into the SM: each warp
@@ -32,7 +33,9 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
   static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int EPI_STAGE_BYTES = 4 * 2 * 32 * 32 * 4;  // 4 warps x 2 buffers x [32][32] fp32
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int EPI_STAGE_BYTES = EPI_WARPS * 32 * 32 * 4;  // one [32][32] fp32 tile per epilogue warp
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + BAR_BYTES + 1024;
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
@@ -40,7 +43,7 @@ struct GemmCfg {
 };
 
 template <int BN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmR, const EpiParams ep, int M, int N, int K,
                         int kb_period, int* status) {
@@ -69,7 +72,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], Cfg::EPI_WARPS);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
     fence_barrier_init();
@@ -151,11 +154,12 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp >= 2) {
     // ---------------------------------------------------------------- epilogue
     const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad + 32) belong to this warp
+    const int ehalf = (warp - 2) >> 2;  // which half of the tile's 32-column chunks
+    constexpr int CH = BN / 32 / 2;     // chunks per epilogue warp
     const bool tma_resid = ep.kind == EPI_RESID;
-    float* stage = reinterpret_cast<float*>(epi_stage + quad * (2 * 32 * 32 * 4));  // 2 x [32][32], 1 KB aligned
+    float* stage = reinterpret_cast<float*>(epi_stage + (warp - 2) * (32 * 32 * 4));  // [32][32], 1 KB aligned
     int acc = 0;
     uint32_t acc_phase = 0;
-    uint32_t nstaged = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int mb = tile / num_n, nb = tile - (tile / num_n) * num_n;
       if (!mbar_wait_warp(&tfull[acc], acc_phase, status, kDevTimeoutGemm)) break;
@@ -164,7 +168,7 @@ __global__ void __launch_bounds__(192, 1)
       const int row = row0 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = ehalf * CH; c < (ehalf + 1) * CH; ++c) {
         uint32_t r[32];
         tmem_ld32(taddr + c * 32, r);
         const int n0 = nb * BN + c * 32;
@@ -174,8 +178,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
             epi_resid_values<32>(ep, row, n0, v);
-            float* buf = stage + (nstaged & 1) * (32 * 32);
-            if (lane == 0) bulk_wait_group_read<1>();  // the reduce that last read `buf` is done
+            float* buf = stage;
+            if (lane == 0) bulk_wait_group_read<0>();  // the reduce that last read `buf` is done
             __syncwarp();
             float4* dst = reinterpret_cast<float4*>(buf + lane * 32);
 #pragma unroll
@@ -187,7 +191,6 @@ __global__ void __launch_bounds__(192, 1)
               tma_reduce_add_2d(&tmR, buf, n0, row0);
               bulk_commit_group();
             }
-            ++nstaged;
           }
         } else if (row < M && n0 < N) {
           float v[32];
@@ -197,7 +200,8 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -225,7 +229,8 @@ static int launch_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensor
   const int tiles = ((M + 127) / 128) * ((N + BN - 1) / BN);
   const int grid = tiles < c.num_sms ? tiles : c.num_sms;
   count_launch(tag, c.stream, true);
-  gemm_bf16_tc_kernel<BN><<<grid, 192, Cfg::SMEM, c.stream>>>(ta, tb, tr, ep, M, N, K, kb_period, c.dev_status);
+  gemm_bf16_tc_kernel<BN><<<grid, Cfg::THREADS, Cfg::SMEM, c.stream>>>(ta, tb, tr, ep, M, N, K, kb_period,
+                                                                       c.dev_status);
   count_launch(tag, c.stream, false);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
