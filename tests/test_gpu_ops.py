@@ -109,6 +109,24 @@ def test_linear_f32(wan, M, N, K):
     assert_f32_close(to_np(out), O.gelu(O.linear(x, w, b)), "linear f32")
 
 
+def test_gelu_epilogue_error_bound(wan):
+    # The GELU epilogue evaluates erf by Abramowitz & Stegun 7.1.26 (|error| <= 1.5e-7)
+    # with SFU reciprocal and exp2.  With an identity weight the GEMM passes x through
+    # exactly, so the output is GELU(x) alone: its error against the exact erf form must
+    # stay within 1e-6 * max(1, |x|) over [-8, 8] (both signs, the tails, and zero).
+    K = 64
+    x = np.linspace(-8.0, 8.0, 512 * K).reshape(512, K).astype(np.float32)
+    x[0, 0] = 0.0
+    w = np.eye(K, dtype=np.float32)
+    out = torch.empty((512, K), dtype=F32, device="cuda")
+    wan.wan_linear(to_dev(x, F32), to_dev(w, F32), None, out, wan.WAN_EPI_GELU)
+    wan.wan_sync_status()
+    g = to_np(out)
+    ref = O.gelu(x.astype(np.float64))
+    err = np.abs(g - ref) / np.maximum(1.0, np.abs(x))
+    assert err.max() <= 1e-6, f"GELU epilogue error {err.max():.2e} at x = {x.flat[err.argmax()]}"
+
+
 # ---------------------------------------------------------------- self-attention with 3D RoPE
 
 ATTN_CASES = [  # (B, grid, H, d)

@@ -358,8 +358,26 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// erf(z) by Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26:
+// for z >= 0, erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2) with
+// t = 1 / (1 + p z), absolute error <= 1.5e-7; odd extension for z < 0.  The reciprocal
+// and exp2 run on the SFU (rcp.approx / ex2.approx, relative error ~2^-22), so the result
+// stays within ~2e-7 of erf: far below the bf16 rounding of the GEMM epilogue outputs.
+__device__ __forceinline__ float erf_as7126(float z) {
+  const float az = fabsf(z);
+  float t;
+  asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(t) : "f"(fmaf(0.3275911f, az, 1.0f)));
+  float poly = fmaf(1.061405429f, t, -1.453152027f);
+  poly = fmaf(poly, t, 1.421413741f);
+  poly = fmaf(poly, t, -0.284496736f);
+  poly = fmaf(poly, t, 0.254829592f);
+  poly *= t;
+  const float e = ex2_approx(-az * az * 1.4426950408889634f);  // exp(-z^2)
+  return copysignf(fmaf(-poly, e, 1.0f), z);
+}
+
 __device__ __forceinline__ float gelu_erf(float x) {
-  return 0.5f * x * (1.0f + erff(x * 0.70710678118654752440f));
+  return 0.5f * x * (1.0f + erf_as7126(x * 0.70710678118654752440f));
 }
 
 }  // namespace wan
