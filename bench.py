@@ -160,6 +160,24 @@ def oracle_step_estimate(s, seed=0, rows_small=128, rows_large=1024):
     return step, threads, sample, sum(times.values())
 
 
+# ---------------------------------------------------------------- multi-rank bookkeeping
+
+def max_over_ranks(value: float, device="cpu") -> float:
+    """The slowest rank's value (every rank gets it); identity without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(units_per_rank_step: float, steps: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return units_per_rank_step * steps * world / (ms_max / 1e3)
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(a, s):
@@ -223,11 +241,7 @@ def run_ours(a, s):
     launches = wan.wan_launch_count() - launches0
     clk = clocks.stop()
     wan.wan_sync_status()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
 
     # ---- end to end through the public API with host buffers (copies inside the timed region)
     x_out_h = torch.empty_like(lat_h).pin_memory()
@@ -252,14 +266,10 @@ def run_ours(a, s):
         step_host()
     f1.record(stream)
     torch.cuda.synchronize(dev)
-    ms_e2e = f0.elapsed_time(f1)
-    if world > 1:
-        tt = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_e2e = float(tt.item())
+    ms_e2e = max_over_ranks(f0.elapsed_time(f1), dev)
 
     tokens_per_step = s.batch * s.tokens
-    value = tokens_per_step * a.steps * world / (ms / 1e3)
+    value = aggregate_rate(tokens_per_step, a.steps, world, ms)
     macs = step_macs(s)
     flop_step = 2 * sum(macs.values())
     pk, pk_kind = peaks()
@@ -294,7 +304,7 @@ def run_ours(a, s):
         "bf16_sustained_frac": round(tflops / pk["bf16_tflops_sustained"], 4),
         "flop_per_step": flop_step,
         "roofline": roof,
-        "e2e": {"value": round(tokens_per_step * a.steps * world / (ms_e2e / 1e3), 1), "unit": UNIT,
+        "e2e": {"value": round(aggregate_rate(tokens_per_step, a.steps, world, ms_e2e), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk,

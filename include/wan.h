@@ -80,6 +80,13 @@ int wan_sync_status(wan_stream_t stream);
 /* Number of libwan kernels launched by this process so far (all devices). */
 long long wan_launch_count(void);
 
+/* Failure-path self-test (no counterpart in the pages): enqueues one kernel whose only
+ * pipeline wait is on a barrier nothing arrives on.  The bounded wait gives up after
+ * limit_ms (1..1000) and records a timeout in the device status word, exactly as a
+ * stalled pipeline would; the next wan_sync_status returns WAN_ERR_TIMEOUT and clears
+ * it.  Nothing faults, traps or hangs; the context stays usable. */
+int wan_watchdog_selftest(int limit_ms, wan_stream_t stream);
+
 /* ------------------------------------------------------------------ patchify
  * [Method] patchify: a 3D conv with kernel = stride = (1,2,2) maps the latent
  * [B, C, F, H, W] to the token sequence x [B, L, D], L = F*(H/2)*(W/2):

@@ -463,6 +463,13 @@ int wan_sync_status(wan_stream_t stream) {
 
 long long wan_launch_count(void) { return g_launches.load(); }
 
+int wan_watchdog_selftest(int limit_ms, wan_stream_t stream) {
+  if (limit_ms < 1 || limit_ms > 1000) return WAN_ERR_INVALID_ARG;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  return launch_watchdog_selftest(c, (unsigned long long)limit_ms * 1000000ull);
+}
+
 size_t wan_patchify_workspace_size(int B, int C, int F, int H, int W, int dtype) {
   if (B <= 0 || C <= 0 || F <= 0 || H <= 0 || W <= 0) return 0;
   return patch_ws_bytes(B, C, F, H, W, dtype == WAN_F32);

@@ -394,4 +394,24 @@ int launch_schedule(const LaunchCtx& c, float* ts, int steps) {
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------ watchdog self-test
+// One thread waits, through the same bounded wait every pipeline uses, on an mbarrier
+// that nothing ever arrives on; after limit_ns it records a timeout in the device status
+// word and returns.  Exercises the failure path without faulting or hanging the GPU.
+__global__ void watchdog_selftest_kernel(unsigned long long limit_ns, int* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    mbar_wait_for(&bar, 0, status, kDevTimeoutSelftest, limit_ns);
+  }
+}
+
+int launch_watchdog_selftest(const LaunchCtx& c, unsigned long long limit_ns) {
+  count_launch("watchdog_selftest", c.stream, true);
+  watchdog_selftest_kernel<<<1, 32, 0, c.stream>>>(limit_ns, c.dev_status);
+  count_launch("watchdog_selftest", c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
 }  // namespace wan

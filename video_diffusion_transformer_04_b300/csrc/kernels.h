@@ -71,6 +71,8 @@ int launch_block_mods(const LaunchCtx& c, const float* e0, const void* const* mo
 int launch_rope_apply(const LaunchCtx& c, const void* in, void* out, const RopeGeom& g, int B, int L, int H, int d,
                       int in_type);
 int launch_schedule(const LaunchCtx& c, float* ts, int steps);
+// A kernel whose only wait never completes: it gives up after limit_ns (status word set).
+int launch_watchdog_selftest(const LaunchCtx& c, unsigned long long limit_ns);
 
 // RoPE table geometry for head_dim d on grid (Fg, Hg, Wg).
 inline RopeGeom rope_geom(const float* omega, int Fg, int Hg, int Wg, int d) {

@@ -19,6 +19,7 @@ enum DevStatus : int {
   kDevOk = 0,
   kDevTimeoutGemm = 0x101,
   kDevTimeoutAttn = 0x102,
+  kDevTimeoutSelftest = 0x1ff,
 };
 
 // A pipeline wait gives up after this much wall time (globaltimer, ns).  Every wait in
@@ -87,9 +88,10 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 }
 
 // Wait until the phase of `bar` with the given parity has completed.  Gives up (returns
-// false and records `code` in the device status word) after kWaitLimitNs, or as soon as
-// another CTA has recorded a failure.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int code) {
+// false and records `code` in the device status word) after limit_ns of %globaltimer,
+// or as soon as another CTA has recorded a failure.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, int* status, int code,
+                                              unsigned long long limit_ns) {
   if (mbar_test(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   uint32_t n = 0;
@@ -97,12 +99,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     if (mbar_test(bar, parity)) return true;
     if ((++n & 1023u) == 0) {
       if (*reinterpret_cast<volatile int*>(status) != 0) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         atomicCAS(status, 0, code);
         return false;
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int code) {
+  return mbar_wait_for(bar, parity, status, code, kWaitLimitNs);
 }
 
 // Warp-uniform variant for roles where every lane waits (epilogue, softmax): the

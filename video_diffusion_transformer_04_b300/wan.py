@@ -63,6 +63,7 @@ _SIGS = {
     "wan_status_string": (C.c_char_p, [I]),
     "wan_sync_status": (I, [P]),
     "wan_launch_count": (LL, []),
+    "wan_watchdog_selftest": (I, [I, P]),
     "wan_patchify_workspace_size": (SZ, [I, I, I, I, I, I]),
     "wan_patchify": (I, [P, P, P, P, I, I, I, I, I, I, I, P, SZ, P]),
     "wan_adaln_modulate": (I, [P, P, P, P, I, I, I, F, I, P]),
@@ -136,6 +137,10 @@ def wan_sync_status(stream=None):
 
 def wan_launch_count() -> int:
     return lib.wan_launch_count()
+
+
+def wan_watchdog_selftest(limit_ms=50, stream=None):
+    _check(lib.wan_watchdog_selftest(limit_ms, _stream(stream)), "wan_watchdog_selftest")
 
 
 def wan_patchify(latent, w, b, x, ws, stream=None):
