@@ -127,12 +127,15 @@ def blas_threads() -> int:
     return len(os.sched_getaffinity(0))
 
 
-def oracle_step_estimate(s, seed=0, rows_small=128, rows_large=1024):
+def oracle_step_estimate(s, seed=0, rows_small=1, rows_large=2049):
     """Time the fp64 oracle on a bounded sample of one block and extrapolate to a step.
 
-    Sample: one 1.3B-shaped block on batch entry 0 with every key/value row (LN, QKV over
-    all L tokens) and `rows` query rows through attention, cross-attention and the FFN,
-    at two row counts; block time = fixed + L * per_row; step = batch * blocks * block.
+    Sample: one 1.3B-shaped block on batch entry 0, run twice: with `rows_small` query
+    rows (the row-independent part: LN and the key/value projections over all L tokens)
+    and with `rows_large` rows (plus that many rows through attention over all keys,
+    cross-attention and the FFN).  per_row = the difference / (rows_large - rows_small),
+    measured over thousands of rows so it is not lost in the fixed part's noise; block =
+    fixed + L * per_row; step = batch * blocks * block.
     """
     from oracle import wan_oracle as O
     one = s.replace(blocks=1)
@@ -354,7 +357,7 @@ def run_reference(a, s):
     est = []
     threads, sample = 1, ""
     for i in range(a.warmup + a.steps):
-        step_s, threads, sample, _ = oracle_step_estimate(s, rows_small=16, rows_large=64)
+        step_s, threads, sample, _ = oracle_step_estimate(s, rows_small=1, rows_large=513)
         if i >= a.warmup:
             est.append(step_s)
     step_s = statistics.mean(est)

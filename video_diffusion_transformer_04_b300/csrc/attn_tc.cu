@@ -8,7 +8,11 @@
 // output accumulator O (d fp32 columns): 2 x 256 = 512 columns.
 //   warp 0      TMA: Q once, then K and V tiles into 2-deep rings
 //   warp 1      tcgen05.mma from one thread: S_i = Q_i K^T (both operands in smem),
-//               O_i += P_i V (P from TMEM, V tile from smem), ping-ponging the tiles
+//               O_i += P_i V (P from TMEM, V tile from smem), ping-ponging the tiles.
+//               Per key tile j: PV_0(j); then S_0(j+1) and PV_1(j) interleaved MMA by
+//               MMA (the smem-bound SS product alternating with the TMEM-fed TS product
+//               keeps both operand paths busy); then S_1(j+1).  S_i(j+1) always follows
+//               PV_i(j), because P_i overwrites S_i in TMEM.
 //   warps 4..11 softmax, one warpgroup per query tile, one thread per query row: fp32
 //               running max and sum, exp2 on the MUFU unit, lazy rescale of O in TMEM
 //               only when the running max grows by more than 2^8, final 1/l and store.
@@ -47,6 +51,7 @@ struct AttnCfg {
   static constexpr int PRODUCER_REGS = 56;
   static constexpr int SOFTMAX_REGS = 224;
   static_assert(128 * PRODUCER_REGS + 256 * SOFTMAX_REGS <= 384 * 168, "register split");
+  static_assert(HD % 64 == 0 && HD <= BKV, "the interleaved S/PV issue assumes HD/16 <= BKV/16 K steps");
 };
 
 struct AttnParams {
@@ -193,21 +198,41 @@ __global__ void __launch_bounds__(384, 1)
     for (int j = 0; j < nkv && ok; ++j) {
       const int vs = j & 1;
       const int ks = (j + 1) & 1;
+      const bool more = j + 1 < nkv;
       if (!mbar_wait(&v_full[vs], (j >> 1) & 1, status, kDevTimeoutAttn)) { ok = false; break; }
-      for (int i = 0; i < ntile; ++i) {
-        if (!mbar_wait(&p_ready[i], j & 1, status, kDevTimeoutAttn)) { ok = false; break; }
+      if (more && !mbar_wait(&k_full[ks], ((j + 1) >> 1) & 1, status, kDevTimeoutAttn)) { ok = false; break; }
+      if (!mbar_wait(&p_ready[0], j & 1, status, kDevTimeoutAttn)) { ok = false; break; }
+      tc_fence_after();
+      issue_PV(0, vs, j > 0 ? 1u : 0u);
+      if (ntile == 2) {
+        if (!mbar_wait(&p_ready[1], j & 1, status, kDevTimeoutAttn)) { ok = false; break; }
         tc_fence_after();
-        issue_PV(i, vs, j > 0 ? 1u : 0u);
-        if (i == ntile - 1) tc_commit(&v_empty[vs]);
-        if (j + 1 < nkv) {
-          if (i == 0) {
-            if (!mbar_wait(&k_full[ks], ((j + 1) >> 1) & 1, status, kDevTimeoutAttn)) { ok = false; break; }
-            tc_fence_after();
+        // S_0(j+1) (both operands in smem) interleaved with PV_1(j) (A in TMEM).
+        const uint32_t va = vs ? v_lo1 : v_lo0;
+        const uint32_t ka = ks ? k_lo1 : k_lo0;
+#pragma unroll
+        for (int kk = 0; kk < Cfg::BKV / 16; ++kk) {  // PV: BKV/16 key steps; S: HD/16 <= BKV/16 steps
+          if (more && kk < HD / 16) {
+            const uint32_t off = ((kk >> 2) * Cfg::Q_BOX + (kk & 3) * 32) >> 4;
+            tc_mma_ss_lo(tmem_base, q_lo0 + off, ka + off, idS, kk > 0 ? 1u : 0u);
           }
-          issue_S(i, ks);
-          if (i == ntile - 1) tc_commit(&k_empty[ks]);
+          const uint32_t voff = (kk * 16 * 128) >> 4;
+          tc_mma_ts_lo(tmem_base + 256 + 128, tmem_base + 256 + kk * 8, va + voff, idO, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(&s_full[i]);  // S_{i,j+1} ready, or (last j) O_i final
+        tc_commit(&v_empty[vs]);
+        tc_commit(&s_full[0]);
+        if (more) {
+          issue_S(1, ks);
+          tc_commit(&k_empty[ks]);
+        }
+        tc_commit(&s_full[1]);
+      } else {
+        tc_commit(&v_empty[vs]);
+        if (more) {
+          issue_S(0, ks);
+          tc_commit(&k_empty[ks]);
+        }
+        tc_commit(&s_full[0]);
       }
     }
     if (!ok) {
