@@ -167,6 +167,25 @@ def test_attn_rope3d_bf16(wan, B, grid, H, d, rope, qkt):
         assert_bf16_close(to_np(o[b]), O.attention(qq, kk, v[b]), f"attn b={b}")
 
 
+@pytest.mark.parametrize("qkt", ["bf16", "f16"])
+def test_attn_rising_row_max_rescales(wan, qkt):
+    # Keys grow tile by tile, so each query row's max logit rises by far more than the
+    # kernel's lazy-rescale threshold after the first key tile: the rescale path (new
+    # reference max, O and row sum scaled, exponentials redone) runs on most rows.
+    B, L, H, d = 1, 4 * 128 + 37, 2, 128
+    q, k, v = _attn_inputs(13, B, L, H, d, True)
+    growth = (0.2 + 1.2 * (np.arange(L) // 128)).astype(np.float32)
+    k = rb(k * growth[None, :, None, None])
+    o = torch.full((B, L, H, d), float("nan"), dtype=BF, device="cuda")
+    QK = BF if qkt == "bf16" else torch.float16
+    wan.wan_attn_rope3d(to_dev(q, QK), to_dev(k, QK), to_dev(v, BF), o, (1, 1, L), apply_rope=False)
+    wan.wan_sync_status()
+    logits = np.einsum("lhd,mhd->hlm", q[0], k[0]) / np.sqrt(d)
+    first = logits[:, :, :128].max(axis=2)
+    assert np.mean(logits.max(axis=2) - first > 9.0 / np.log2(np.e)) > 0.5  # the path is exercised
+    assert_bf16_close(to_np(o[0]), O.attention(q[0], k[0], v[0]), "attention with rising row max")
+
+
 def test_attn_rope3d_f32(wan):
     B, grid, H, d = 2, (3, 4, 5), 2, 64
     L = 60

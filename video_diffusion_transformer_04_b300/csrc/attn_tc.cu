@@ -19,15 +19,14 @@
 // The first warpgroup (TMA, MMA, two idle warps) gives registers to the softmax
 // warpgroups (setmaxnreg), which keep a whole 128-column score row in registers.
 // Per score element the softmax issues half an FFMA2 (scale and max subtraction on
-// packed pairs), one MUFU ex2, half a bf16x2 pack, half an FADD2 (row sum) and half a
-// 3-input max; the ragged-tile mask runs only on the last key tile.
+// packed pairs), one MUFU ex2, half a bf16x2 pack and half an FADD2 (row sum); the row
+// max is only computed for the first key tile and when a row sum signals that the
+// reference max must move; the ragged-tile mask runs only on the last key tile.
 // V is read in its natural [token, H*d] layout: in the PV product it is the B operand
 // with N = d contiguous, i.e. MN-major (descriptor LBO = the 64-column box stride,
 // SBO = 1024 bytes per 8 keys), so no transposed copy of V is ever written.
 // Ragged tails: keys past Lkv are zero-filled by TMA and masked to -inf; query rows
 // past Lq are computed on zero rows and not stored.
-#include <type_traits>
-
 #include "kernels.h"
 #include "wan_common.cuh"
 
@@ -266,28 +265,17 @@ __global__ void __launch_bounds__(384, 1)
             if (e >= valid) sr[e] = __float_as_uint(-INFINITY);
         }
       };
-      // p = 2^(s * scale - m) on packed pairs (FFMA2, MUFU ex2), written as bf16x2 into
-      // the first half of each 32-column chunk's registers (dead once read); row sum in
-      // FADD2 accumulators on the fp32 values.  TRACK also returns the row max of s from
-      // the same reads (3-input max chains), off the exp dependency chain.
-      auto exp_pass = [&](auto track, float m, float& rowsum) -> float {
-        constexpr bool TRACK = decltype(track)::value;
+      // p = 2^(s * scale - m): packed pairs through FFMA2, exp2 on MUFU, bf16x2 into the
+      // first half of each 32-column chunk's registers (dead once read), row sum in
+      // four FADD2 accumulators on the fp32 values.
+      auto exp_pass = [&](float m, float& rowsum) {
         const uint64_t negm = f2_pack(-m, -m);
         uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float s0 = __uint_as_float(sr[c * 32 + 2 * e]), s1 = __uint_as_float(sr[c * 32 + 2 * e + 1]);
-            if constexpr (TRACK) {
-              switch (e & 3) {
-                case 0: mx0 = fmax3(mx0, s0, s1); break;
-                case 1: mx1 = fmax3(mx1, s0, s1); break;
-                case 2: mx2 = fmax3(mx2, s0, s1); break;
-                default: mx3 = fmax3(mx3, s0, s1); break;
-              }
-            }
             const float2 t = f2_unpack(f2_fma(f2_pack(s0, s1), sl2x2, negm));
             const float p0 = ex2_approx(t.x), p1 = ex2_approx(t.y);
             sr[c * 32 + e] = pack_bf16x2(p0, p1);
@@ -302,6 +290,20 @@ __global__ void __launch_bounds__(384, 1)
         }
         const float2 rs = f2_unpack(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)));
         rowsum = rs.x + rs.y;
+      };
+      // Row max of the scores in sr (four chains of 3-input max).
+      auto row_max = [&]() -> float {
+        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+#pragma unroll
+        for (int e = 4; e < Cfg::BKV - 4; e += 8) {
+          mx0 = fmax3(mx0, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
+          mx2 = fmax3(mx2, __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
+          mx3 = fmax3(mx3, __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
+        }
+        mx0 = fmax3(mx0, __uint_as_float(sr[Cfg::BKV - 4]), __uint_as_float(sr[Cfg::BKV - 3]));
+        mx1 = fmax3(mx1, __uint_as_float(sr[Cfg::BKV - 2]), __uint_as_float(sr[Cfg::BKV - 1]));
         return fmax3(mx0, mx1, fmaxf(mx2, mx3));
       };
       for (int j = 0; j < nkv; ++j) {
@@ -312,28 +314,21 @@ __global__ void __launch_bounds__(384, 1)
         float rowsum;
         if (j == 0) {
           // First key tile: the reference max is this tile's row max.
-          float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-          float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
-#pragma unroll
-          for (int e = 4; e < Cfg::BKV - 4; e += 8) {
-            mx0 = fmax3(mx0, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
-            mx1 = fmax3(mx1, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
-            mx2 = fmax3(mx2, __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
-            mx3 = fmax3(mx3, __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
-          }
-          mx0 = fmax3(mx0, __uint_as_float(sr[Cfg::BKV - 4]), __uint_as_float(sr[Cfg::BKV - 3]));
-          mx1 = fmax3(mx1, __uint_as_float(sr[Cfg::BKV - 2]), __uint_as_float(sr[Cfg::BKV - 1]));
-          m_used = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
-          exp_pass(std::false_type{}, m_used, rowsum);
+          m_used = row_max() * sl2;
+          exp_pass(m_used, rowsum);
         } else {
-          // Lazy rescale: exponentiate against the current reference max and track the
-          // tile max on the way.  Only when some row's tile max exceeds its reference by
-          // more than 8 (a factor 256 in the exponentials) does the warp move those rows'
-          // reference, rescale their O and sum (alpha = 1 for the other rows: the
-          // tcgen05.ld/st are warp-collective), reload S and redo the exponentials.
-          const float mt = exp_pass(std::true_type{}, m_used, rowsum) * sl2;
-          const bool need = mt > m_used + 8.0f;
+          // Lazy rescale: exponentiate against the current reference max.  A tile row sum
+          // above 2^16 means some exponential exceeded 2^9 (128 keys), i.e. the row's max
+          // rose by more than 9 (log2) since its reference was set: only then does the warp
+          // find those rows' new max, rescale their O and sum (alpha = 1 for the other rows:
+          // the tcgen05.ld/st are warp-collective), reload S and redo the exponentials.
+          // Otherwise every p <= 2^16, which bf16 P and the fp32 O and sum hold as well as
+          // p <= 1.  (An overflow to inf or a NaN also takes the slow path.)
+          exp_pass(m_used, rowsum);
+          const bool need = !(rowsum <= 65536.0f);
           if (__any_sync(0xffffffffu, need)) {
+            load_scores(valid);
+            const float mt = row_max() * sl2;
             const float alpha = need ? ex2_approx(m_used - mt) : 1.0f;
             l_sum *= alpha;
             if (need) m_used = mt;
@@ -345,8 +340,7 @@ __global__ void __launch_bounds__(384, 1)
               for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
               tmem_st32(tO + c * 32, orr);
             }
-            load_scores(valid);
-            exp_pass(std::false_type{}, m_used, rowsum);
+            exp_pass(m_used, rowsum);
           }
         }
 #pragma unroll

@@ -114,6 +114,10 @@ def _stream(stream=None):
     return s.cuda_stream
 
 
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
 def _check(st, where):
     if st != WAN_OK:
         raise WanError(st, where)
@@ -168,19 +172,19 @@ def wan_attn_rope3d(q, k, v, o, grid, theta=10000.0, apply_rope=True, ws=None, s
     B, L, H, d = q.shape
     _check(lib.wan_attn_rope3d(_p(q), _p(k), _p(v), _p(o), B, L, H, d, grid[0], grid[1], grid[2], theta,
                                1 if apply_rope else 0, dtype_code(v.dtype), dtype_code(q.dtype), _p(ws),
-                               ws.numel() * ws.element_size(), _stream(stream)), "wan_attn_rope3d")
+                               _nbytes(ws), _stream(stream)), "wan_attn_rope3d")
 
 
 def wan_cross_attn_workspace_size(B, Lt, Li, H, d, dtype):
     return lib.wan_cross_attn_workspace_size(B, Lt, Li, H, d, dtype)
 
 
-def wan_cross_attn(q, kt, vt, ki, vi, o, ws, stream=None):
+def wan_cross_attn(q, kt, vt, ki, vi, o, ws=None, stream=None):
     B, L, H, d = q.shape
     Lt = kt.shape[1]
     Li = ki.shape[1] if ki is not None else 0
     _check(lib.wan_cross_attn(_p(q), _p(kt), _p(vt), _p(ki), _p(vi), _p(o), B, L, Lt, Li, H, d, dtype_code(vt.dtype),
-                              dtype_code(q.dtype), _p(ws), ws.numel() * ws.element_size(), _stream(stream)),
+                              dtype_code(q.dtype), _p(ws), _nbytes(ws), _stream(stream)),
            "wan_cross_attn")
 
 
