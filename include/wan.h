@@ -116,13 +116,17 @@ int wan_adaln_modulate(const float* x, const float* shift, const float* scale, v
  * v, o: [B, L, H, d] in dtype; q, k: [B, L, H, d] in qk_dtype (= dtype, or WAN_F16 with
  * dtype WAN_BF16).  apply_rope = 0 treats q and k as already rotated.  With dtype
  * WAN_BF16 the rotated q and k enter the QK^T product in fp16.
+ * kv_lens: DEVICE int [B] or NULL.  [Code] flash_attention(..., k_lens=seq_lens): entry b
+ * attends to its first kv_lens[b] keys only (values outside [1, L] are clamped to that
+ * range); keys past that length must hold finite values (they get weight exactly 0).
+ * NULL: every entry attends to all L keys.
  * ws (the rotated q and k): >= wan_attn_workspace_size(...) bytes, 1024-byte aligned;
  * unused (may be NULL) when apply_rope = 0.  d must be 64 or 128 (bf16 path); d <= 128
  * and even (fp32 path). */
 size_t wan_attn_workspace_size(int B, int L, int H, int d, int dtype);
-int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B, int L, int H, int d,
-                    int Fg, int Hg, int Wg, float theta, int apply_rope, int dtype, int qk_dtype,
-                    void* ws, size_t ws_bytes, wan_stream_t stream);
+int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, const int* kv_lens, int B,
+                    int L, int H, int d, int Fg, int Hg, int Wg, float theta, int apply_rope, int dtype,
+                    int qk_dtype, void* ws, size_t ws_bytes, wan_stream_t stream);
 
 /* ------------------------------------------------------------------ cross-attention
  * [Method] text conditioning by cross-attention; [I2V] decoupled cross-attention to the
@@ -131,12 +135,15 @@ int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B,
  * o: [B, L, H, d]; vt: [B, Lt, H, d]; vi: [B, Li, H, d] or NULL (dtype).
  * q: [B, L, H, d]; kt: [B, Lt, H, d]; ki: [B, Li, H, d] or NULL (qk_dtype: dtype, or
  * WAN_F16 with dtype WAN_BF16).
+ * kt_lens: DEVICE int [B] or NULL: valid text tokens per entry of a padded context (the
+ * k_lens of [Code]; clamped to [1, Lt]; padded keys must be finite); the image segment
+ * is always fully valid.
  * ws, ws_bytes: unused (wan_cross_attn_workspace_size returns 0; q, k, v are read in
  * place), kept so a caller can pass the same workspace to every attention call. */
 size_t wan_cross_attn_workspace_size(int B, int Lt, int Li, int H, int d, int dtype);
-int wan_cross_attn(const void* q, const void* kt, const void* vt, const void* ki, const void* vi,
-                   void* o, int B, int L, int Lt, int Li, int H, int d, int dtype, int qk_dtype,
-                   void* ws, size_t ws_bytes, wan_stream_t stream);
+int wan_cross_attn(const void* q, const void* kt, const void* vt, const int* kt_lens, const void* ki,
+                   const void* vi, void* o, int B, int L, int Lt, int Li, int H, int d, int dtype,
+                   int qk_dtype, void* ws, size_t ws_bytes, wan_stream_t stream);
 
 /* ------------------------------------------------------------------ FFN
  * FFN sub-layer with gated residual: x += gate[b] * (W2 GELU(W1 y + b1) + b2).
@@ -253,29 +260,31 @@ int wan_time_embed(const wan_dit_config* cfg, const wan_dit_weights* w, const fl
  * decoupled ctx_img), AdaLN-modulated GELU FFN, gated residuals) -> head -> depatchify.
  * latent: fp32 [B, c_in, F, H, W], or [1, ...] broadcast to every batch entry when
  * latent_broadcast != 0; t: fp32 [B] DEVICE timesteps in [0, 1]; ctx_txt: [B, Lt, D];
- * ctx_img: [B, Li, D] or NULL (dtype); v_out: fp32 [B, c_out, F, H, W].
+ * txt_lens: DEVICE int [B] valid text tokens per entry of a padded ctx_txt, or NULL (all
+ * Lt valid); ctx_img: [B, Li, D] or NULL (dtype); v_out: fp32 [B, c_out, F, H, W].
  * ws: >= wan_dit_workspace_size(cfg) bytes, 1024-byte aligned. */
 int wan_dit_forward(const wan_dit_config* cfg, const wan_dit_weights* w, const float* latent,
-                    int latent_broadcast, const float* t, const void* ctx_txt, const void* ctx_img,
-                    float* v_out, void* ws, size_t ws_bytes, wan_stream_t stream);
+                    int latent_broadcast, const float* t, const void* ctx_txt, const int* txt_lens,
+                    const void* ctx_img, float* v_out, void* ws, size_t ws_bytes, wan_stream_t stream);
 
 /* One guided denoising step (cfg->batch must be 2: cond, uncond).  Runs the DiT on
  * [cond; uncond] with the shared latent x and timestep, then fuses CFG and the Euler
  * update into x's first c_out channels.  x: fp32 [1, c_in, F, H, W] in/out;
- * t_pair: fp32 DEVICE {t, t_next}; ctx_txt: [2, Lt, D] (cond first); ctx_img: [2, Li, D]
- * or NULL.  v_ws: fp32 [2, c_out, F, H, W] receives the two velocity predictions. */
+ * t_pair: fp32 DEVICE {t, t_next}; ctx_txt: [2, Lt, D] (cond first); txt_lens: DEVICE int
+ * [2] or NULL; ctx_img: [2, Li, D] or NULL.  v_ws: fp32 [2, c_out, F, H, W] receives the
+ * two velocity predictions. */
 int wan_dit_guided_step(const wan_dit_config* cfg, const wan_dit_weights* w, float* x,
                         const float* t_pair, float guide_scale, const void* ctx_txt,
-                        const void* ctx_img, float* v_ws, void* ws, size_t ws_bytes,
-                        wan_stream_t stream);
+                        const int* txt_lens, const void* ctx_img, float* v_ws, void* ws,
+                        size_t ws_bytes, wan_stream_t stream);
 
 /* [Sampler 3.2, 4.4] End-to-end Euler sampling: `steps` guided steps on the uniform
  * schedule t_k = 1 - k/steps, from noise x (t = 1) to the data estimate (t = 0).
  * t_sched: fp32 DEVICE scratch of steps+1 floats; other arguments as for
  * wan_dit_guided_step. */
 int wan_sample(const wan_dit_config* cfg, const wan_dit_weights* w, float* x, int steps,
-               float guide_scale, const void* ctx_txt, const void* ctx_img, float* t_sched,
-               float* v_ws, void* ws, size_t ws_bytes, wan_stream_t stream);
+               float guide_scale, const void* ctx_txt, const int* txt_lens, const void* ctx_img,
+               float* t_sched, float* v_ws, void* ws, size_t ws_bytes, wan_stream_t stream);
 
 /* ------------------------------------------------------------------ profiling
  * Kernel timing with CUDA events recorded around every libwan launch while enabled.

@@ -73,11 +73,11 @@ def test_host_validation_rejects_bad_arguments(wanlib):
     assert g(1 << 12, 1 << 12, None, 1 << 12, 8, 64, 64, 0, None, 0, 1, 2, None) == -2
     assert g(1 << 12, 1 << 12, None, 1 << 12, 8, 64, 64, 2, None, 0, 0, 2, None) == -2
     h = wanlib.wan_cross_attn
-    h.argtypes = [C.c_void_p] * 6 + [C.c_int] * 8 + [C.c_void_p, C.c_size_t, C.c_void_p]
+    h.argtypes = [C.c_void_p] * 7 + [C.c_int] * 8 + [C.c_void_p, C.c_size_t, C.c_void_p]
     # q/k in fp16 are accepted only next to bf16 v/o; unknown codes are invalid
-    assert h(None, None, None, None, None, None, 1, 8, 8, 0, 1, 64, 1, 2, None, 0, None) == -2
-    assert h(None, None, None, None, None, None, 1, 8, 8, 0, 1, 64, 0, 5, None, 0, None) == -1
-    assert h(None, None, None, None, None, None, 1, 8, 8, 0, 1, 64, 0, 2, None, 0, None) == -1  # NULL q
+    assert h(None, None, None, None, None, None, None, 1, 8, 8, 0, 1, 64, 1, 2, None, 0, None) == -2
+    assert h(None, None, None, None, None, None, None, 1, 8, 8, 0, 1, 64, 0, 5, None, 0, None) == -1
+    assert h(None, None, None, None, None, None, None, 1, 8, 8, 0, 1, 64, 0, 2, None, 0, None) == -1  # NULL q
 
 
 def test_dit_workspace_size_arithmetic():

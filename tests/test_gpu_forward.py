@@ -60,6 +60,27 @@ def test_tiny_guided_step(wan, dtype):
         assert_bf16_close(to_np(x), x_o, "x_next")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tiny_forward_padded_text(wan, dtype):
+    # Padded text contexts with per-entry valid lengths (k_lens of the cross-attention):
+    # the result must equal the oracle run on each entry's unpadded context.
+    s = synth.CONFIGS[0].replace(dtype=dtype)
+    w, inp, m = _model(wan, s)
+    tdt = m.tdtype
+    ctx = m.text_embed(to_dev(inp["text"], tdt))
+    lens = np.array([5, 16], np.int32)
+    lat = np.concatenate([inp["latent"], 0.5 * inp["latent"]], axis=0)
+    t = np.array([0.3, 0.8], np.float32)
+    v = m.forward(to_dev(lat, F32), to_dev(t, F32), ctx, txt_lens=torch.from_numpy(lens).cuda())
+    wan.wan_sync_status()
+    ctx_o = O.text_projection(inp["text"], w)
+    v_o = O.dit_forward(lat, t, [ctx_o[b, :lens[b]] for b in range(2)], None, w, s)
+    if dtype == "f32":
+        assert_f32_close(to_np(v), v_o, "v with padded text")
+    else:
+        assert_bf16_close(to_np(v), v_o, "v with padded text")
+
+
 def test_tiny_forward_batch_permutation(wan):
     # Permuting the batch (latents, timesteps, contexts) permutes the outputs.
     s = synth.CONFIGS[0]

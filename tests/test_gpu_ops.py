@@ -186,6 +186,29 @@ def test_attn_rising_row_max_rescales(wan, qkt):
     assert_bf16_close(to_np(o[0]), O.attention(q[0], k[0], v[0]), "attention with rising row max")
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+def test_attn_kv_lens(wan, dt):
+    # k_lens: entry b attends to its first kv_lens[b] keys; the padded keys hold finite
+    # random values that must get exactly zero weight.  Lengths: one key, one key past a
+    # tile, and the full (ragged) sequence.
+    B, L, H, d = 3, 300, 2, 64 if dt == "f32" else 128
+    lens = np.array([1, 129, 300], np.int32)
+    q, k, v = _attn_inputs(14, B, L, H, d, dt != "f32")
+    o = torch.full((B, L, H, d), float("nan"), dtype=F32 if dt == "f32" else BF, device="cuda")
+    QK = {"bf16": BF, "f16": torch.float16, "f32": F32}[dt]
+    VT = F32 if dt == "f32" else BF
+    wan.wan_attn_rope3d(to_dev(q, QK), to_dev(k, QK), to_dev(v, VT), o, (1, 1, L), apply_rope=False,
+                        kv_lens=torch.from_numpy(lens).cuda())
+    wan.wan_sync_status()
+    for b in range(B):
+        n = lens[b]
+        ref = O.attention(q[b], k[b, :n], v[b, :n])
+        if dt == "f32":
+            assert_f32_close(to_np(o[b]), ref, f"k_lens b={b}")
+        else:
+            assert_bf16_close(to_np(o[b]), ref, f"k_lens b={b}")
+
+
 def test_attn_rope3d_f32(wan):
     B, grid, H, d = 2, (3, 4, 5), 2, 64
     L = 60
@@ -218,6 +241,26 @@ def test_attn_full_size_sampled_rows(wan):
 
 
 # ---------------------------------------------------------------- cross-attention
+
+def test_cross_attn_text_lens(wan):
+    # Padded text contexts (k_lens of the text keys); the image segment stays fully valid.
+    B, L, Lt, Li, H, d = 2, 130, 512, 257, 2, 128
+    lens = np.array([77, 512], np.int32)
+    q = rb(synth.normal(15, "cl.q", (B, L, H, d)))
+    kt = rb(synth.normal(15, "cl.kt", (B, Lt, H, d)))
+    vt = rb(synth.normal(15, "cl.vt", (B, Lt, H, d)))
+    ki = rb(synth.normal(15, "cl.ki", (B, Li, H, d)))
+    vi = rb(synth.normal(15, "cl.vi", (B, Li, H, d)))
+    o = torch.full((B, L, H, d), float("nan"), dtype=BF, device="cuda")
+    F16 = torch.float16
+    wan.wan_cross_attn(to_dev(q, F16), to_dev(kt, F16), to_dev(vt, BF), to_dev(ki, F16), to_dev(vi, BF), o,
+                       kt_lens=torch.from_numpy(lens).cuda())
+    wan.wan_sync_status()
+    for b in range(B):
+        n = lens[b]
+        ref = O.attention(q[b], kt[b, :n], vt[b, :n]) + O.attention(q[b], ki[b], vi[b])
+        assert_bf16_close(to_np(o[b]), ref, f"cross k_lens b={b}")
+
 
 @pytest.mark.parametrize("B,L,Lt,Li,H,d", [(2, 130, 512, 257, 2, 128), (1, 48, 16, 0, 2, 64), (1, 1, 1, 1, 1, 128)])
 @pytest.mark.parametrize("qkt", ["bf16", "f16"])

@@ -285,7 +285,8 @@ static int time_embed_impl(const LaunchCtx& c, const wan_dit_config* cfg, const 
 
 static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w, const float* latent,
                             long long lat_bstride, const float* t, int t_stride, const void* ctx_txt,
-                            const void* ctx_img, float* v_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                            const int* txt_lens, const void* ctx_img, float* v_out, void* ws, size_t ws_bytes,
+                            cudaStream_t stream) {
   WAN_TRY(validate_cfg(cfg));
   WAN_TRY(validate_weights(cfg, w));
   if (!latent || !t || !ctx_txt || !v_out || (cfg->img_len && !ctx_img)) return WAN_ERR_INVALID_ARG;
@@ -384,6 +385,7 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
       a.o = W.o; a.ldo = D; a.o_col = 0;
       a.B = B; a.Lq = L; a.Lkv = Lk; a.H = H; a.head_dim = hd;
       a.accumulate = seg;
+      a.kv_lens = seg ? nullptr : txt_lens;  // text keys may be padded; the 257 image tokens are all valid
       a.tag = "attn_cross";
       a.qk_f16 = !f32;
       WAN_TRY(attend(c, f32, a));
@@ -508,9 +510,9 @@ size_t wan_attn_workspace_size(int B, int L, int H, int d, int dtype) {
   return (size_t)round_up((long long)bp.off, 1024);
 }
 
-int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B, int L, int H, int d, int Fg, int Hg,
-                    int Wg, float theta, int apply_rope, int dtype, int qk_dtype, void* ws, size_t ws_bytes,
-                    wan_stream_t stream) {
+int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, const int* kv_lens, int B, int L, int H,
+                    int d, int Fg, int Hg, int Wg, float theta, int apply_rope, int dtype, int qk_dtype, void* ws,
+                    size_t ws_bytes, wan_stream_t stream) {
   WAN_TRY(check_dtype(dtype));
   WAN_TRY(check_qk_dtype(dtype, qk_dtype));
   const int f32 = dtype == WAN_F32;
@@ -547,6 +549,7 @@ int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, int B,
   a.v = v; a.ldv = D; a.v_row_len = D;
   a.o = o; a.ldo = D;
   a.B = B; a.Lq = L; a.Lkv = L; a.H = H; a.head_dim = d;
+  a.kv_lens = kv_lens;
   a.tag = "attn_self";
   a.qk_f16 = !f32 && (apply_rope || qk_dtype == WAN_F16);  // rotated q, k are written in fp16
   return attend(c, f32, a);
@@ -557,9 +560,9 @@ size_t wan_cross_attn_workspace_size(int B, int Lt, int Li, int H, int d, int dt
   return 0;  // the kernels read q, k and v in place
 }
 
-int wan_cross_attn(const void* q, const void* kt, const void* vt, const void* ki, const void* vi, void* o, int B,
-                   int L, int Lt, int Li, int H, int d, int dtype, int qk_dtype, void* ws, size_t ws_bytes,
-                   wan_stream_t stream) {
+int wan_cross_attn(const void* q, const void* kt, const void* vt, const int* kt_lens, const void* ki, const void* vi,
+                   void* o, int B, int L, int Lt, int Li, int H, int d, int dtype, int qk_dtype, void* ws,
+                   size_t ws_bytes, wan_stream_t stream) {
   (void)ws, (void)ws_bytes;
   WAN_TRY(check_dtype(dtype));
   WAN_TRY(check_qk_dtype(dtype, qk_dtype));
@@ -582,6 +585,7 @@ int wan_cross_attn(const void* q, const void* kt, const void* vt, const void* ki
     a.o = o; a.ldo = D;
     a.B = B; a.Lq = L; a.Lkv = Lk; a.H = H; a.head_dim = d;
     a.accumulate = seg;
+    a.kv_lens = seg ? nullptr : kt_lens;
     a.tag = "attn_cross";
     a.qk_f16 = qk_dtype == WAN_F16;
     WAN_TRY(attend(c, f32, a));
@@ -716,20 +720,20 @@ int wan_time_embed(const wan_dit_config* cfg, const wan_dit_weights* w, const fl
 }
 
 int wan_dit_forward(const wan_dit_config* cfg, const wan_dit_weights* w, const float* latent, int latent_broadcast,
-                    const float* t, const void* ctx_txt, const void* ctx_img, float* v_out, void* ws, size_t ws_bytes,
-                    wan_stream_t stream) {
+                    const float* t, const void* ctx_txt, const int* txt_lens, const void* ctx_img, float* v_out,
+                    void* ws, size_t ws_bytes, wan_stream_t stream) {
   if (!cfg) return WAN_ERR_INVALID_ARG;
   const long long bstride = latent_broadcast ? 0 : (long long)cfg->c_in * cfg->frames * cfg->height * cfg->width;
-  return dit_forward_impl(cfg, w, latent, bstride, t, 1, ctx_txt, ctx_img, v_out, ws, ws_bytes, stream);
+  return dit_forward_impl(cfg, w, latent, bstride, t, 1, ctx_txt, txt_lens, ctx_img, v_out, ws, ws_bytes, stream);
 }
 
 int wan_dit_guided_step(const wan_dit_config* cfg, const wan_dit_weights* w, float* x, const float* t_pair,
-                        float guide_scale, const void* ctx_txt, const void* ctx_img, float* v_ws, void* ws,
-                        size_t ws_bytes, wan_stream_t stream) {
+                        float guide_scale, const void* ctx_txt, const int* txt_lens, const void* ctx_img, float* v_ws,
+                        void* ws, size_t ws_bytes, wan_stream_t stream) {
   if (!cfg || !x || !t_pair || !v_ws) return WAN_ERR_INVALID_ARG;
   if (cfg->batch != 2) return WAN_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(v_ws)) return WAN_ERR_UNSUPPORTED;
-  WAN_TRY(dit_forward_impl(cfg, w, x, 0, t_pair, 0, ctx_txt, ctx_img, v_ws, ws, ws_bytes, stream));
+  WAN_TRY(dit_forward_impl(cfg, w, x, 0, t_pair, 0, ctx_txt, txt_lens, ctx_img, v_ws, ws, ws_bytes, stream));
   LaunchCtx c;
   WAN_TRY(launch_ctx(stream, &c));
   const long long n = (long long)cfg->c_out * cfg->frames * cfg->height * cfg->width;
@@ -737,14 +741,15 @@ int wan_dit_guided_step(const wan_dit_config* cfg, const wan_dit_weights* w, flo
 }
 
 int wan_sample(const wan_dit_config* cfg, const wan_dit_weights* w, float* x, int steps, float guide_scale,
-               const void* ctx_txt, const void* ctx_img, float* t_sched, float* v_ws, void* ws, size_t ws_bytes,
-               wan_stream_t stream) {
+               const void* ctx_txt, const int* txt_lens, const void* ctx_img, float* t_sched, float* v_ws, void* ws,
+               size_t ws_bytes, wan_stream_t stream) {
   if (!cfg || !x || !t_sched || steps <= 0) return WAN_ERR_INVALID_ARG;
   LaunchCtx c;
   WAN_TRY(launch_ctx(stream, &c));
   WAN_TRY(launch_schedule(c, t_sched, steps));
   for (int k = 0; k < steps; ++k)
-    WAN_TRY(wan_dit_guided_step(cfg, w, x, t_sched + k, guide_scale, ctx_txt, ctx_img, v_ws, ws, ws_bytes, stream));
+    WAN_TRY(wan_dit_guided_step(cfg, w, x, t_sched + k, guide_scale, ctx_txt, txt_lens, ctx_img, v_ws, ws, ws_bytes,
+                                stream));
   return WAN_OK;
 }
 

@@ -25,8 +25,9 @@
 // V is read in its natural [token, H*d] layout: in the PV product it is the B operand
 // with N = d contiguous, i.e. MN-major (descriptor LBO = the 64-column box stride,
 // SBO = 1024 bytes per 8 keys), so no transposed copy of V is ever written.
-// Ragged tails: keys past Lkv are zero-filled by TMA and masked to -inf; query rows
-// past Lq are computed on zero rows and not stored.
+// Ragged tails: keys past the entry's key count (Lkv, or its k_lens value) are masked to
+// -inf (past Lkv TMA also zero-fills them); query rows past Lq are computed on zero rows
+// and not stored.
 #include "kernels.h"
 #include "wan_common.cuh"
 
@@ -62,6 +63,7 @@ struct AttnParams {
   long long ldo;
   int o_col;
   int accumulate;         // o += result (decoupled cross-attention)
+  const int* kv_lens;     // [B] valid keys per batch entry, or NULL (all Lkv)
 };
 
 template <int HD, bool QK_F16>
@@ -93,7 +95,9 @@ __global__ void __launch_bounds__(384, 1)
   const int h = bh - b * p.H;
   const int q0 = qp * 256;
   const int ntile = (q0 + 128 < p.Lq) ? 2 : 1;
-  const int nkv = (p.Lkv + Cfg::BKV - 1) / Cfg::BKV;
+  // Keys of this batch entry: all Lkv, or its own length (k_lens), clamped to [1, Lkv].
+  const int lkv = p.kv_lens ? min(max(p.kv_lens[b], 1), p.Lkv) : p.Lkv;
+  const int nkv = (lkv + Cfg::BKV - 1) / Cfg::BKV;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -309,7 +313,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int j = 0; j < nkv; ++j) {
         if (!mbar_wait_warp(&s_full[i], j & 1, status, kDevTimeoutAttn)) { ok = false; break; }
         tc_fence_after();
-        const int valid = p.Lkv - j * Cfg::BKV;  // >= 1
+        const int valid = lkv - j * Cfg::BKV;  // >= 1
         load_scores(valid);
         float rowsum;
         if (j == 0) {
@@ -443,6 +447,7 @@ int attention_bf16(const LaunchCtx& c, const AttnArgs& a) {
   p.ldo = a.ldo;
   p.o_col = a.o_col;
   p.accumulate = a.accumulate;
+  p.kv_lens = a.kv_lens;
   const char* tag = a.tag ? a.tag : "attn";
   if (HD == 128)
     return a.qk_f16 ? launch_attn<128, true>(c, tq, tk, tv, p, a.B, tag) : launch_attn<128, false>(c, tq, tk, tv, p, a.B, tag);

@@ -42,6 +42,7 @@ struct AttnArgs {
   long long ldo;
   int o_col;
   int B, Lq, Lkv, H, head_dim;
+  const int* kv_lens;  // device [B]: valid keys per batch entry (clamped to [1, Lkv]), or NULL = Lkv
   int accumulate;  // o += result
   int qk_f16;      // bf16 path: q and k are fp16 (else bf16); v and o are bf16
   const char* tag; // profiler label of the launch

@@ -72,10 +72,11 @@ __global__ void __launch_bounds__(256) attn_f32_kernel(const AttnArgs a, float s
     for (int d = lane; d < hd; d += 32) sq[warp][d] = q[((long long)b * a.Lq + row) * a.ldq + a.q_col + h * hd + d];
   __syncwarp();
   if (row >= a.Lq) return;
+  const int lkv = a.kv_lens ? min(max(a.kv_lens[b], 1), a.Lkv) : a.Lkv;
   float m = -INFINITY, l = 0.f;
   float acc[128];
   for (int d = 0; d < hd; ++d) acc[d] = 0.f;
-  for (int j = lane; j < a.Lkv; j += 32) {
+  for (int j = lane; j < lkv; j += 32) {
     const float* kr = k + ((long long)b * a.Lkv + j) * a.ldk + a.k_col + h * hd;
     float s = 0.f;
     for (int d = 0; d < hd; ++d) s = fmaf(sq[warp][d], kr[d], s);

@@ -68,9 +68,9 @@ _SIGS = {
     "wan_patchify": (I, [P, P, P, P, I, I, I, I, I, I, I, P, SZ, P]),
     "wan_adaln_modulate": (I, [P, P, P, P, I, I, I, F, I, P]),
     "wan_attn_workspace_size": (SZ, [I, I, I, I, I]),
-    "wan_attn_rope3d": (I, [P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, P, SZ, P]),
+    "wan_attn_rope3d": (I, [P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, P, SZ, P]),
     "wan_cross_attn_workspace_size": (SZ, [I, I, I, I, I, I]),
-    "wan_cross_attn": (I, [P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, SZ, P]),
+    "wan_cross_attn": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, SZ, P]),
     "wan_ffn": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, P]),
     "wan_linear": (I, [P, P, P, P, I, I, I, I, P, I, I, I, P]),
     "wan_text_embed_workspace_size": (SZ, [I, I, I, I]),
@@ -81,10 +81,11 @@ _SIGS = {
     "wan_dit_workspace_size": (SZ, [C.POINTER(wan_dit_config)]),
     "wan_time_embed_workspace_size": (SZ, [C.POINTER(wan_dit_config)]),
     "wan_time_embed": (I, [C.POINTER(wan_dit_config), C.POINTER(wan_dit_weights), P, I, P, P, P, SZ, P]),
-    "wan_dit_forward": (I, [C.POINTER(wan_dit_config), C.POINTER(wan_dit_weights), P, I, P, P, P, P, P, SZ, P]),
-    "wan_dit_guided_step": (I, [C.POINTER(wan_dit_config), C.POINTER(wan_dit_weights), P, P, F, P, P, P, P, SZ,
-                                P]),
-    "wan_sample": (I, [C.POINTER(wan_dit_config), C.POINTER(wan_dit_weights), P, I, F, P, P, P, P, P, SZ, P]),
+    "wan_dit_forward": (I, [C.POINTER(wan_dit_config), C.POINTER(wan_dit_weights), P, I, P, P, P, P, P, P, SZ,
+                            P]),
+    "wan_dit_guided_step": (I, [C.POINTER(wan_dit_config), C.POINTER(wan_dit_weights), P, P, F, P, P, P, P, P,
+                                SZ, P]),
+    "wan_sample": (I, [C.POINTER(wan_dit_config), C.POINTER(wan_dit_weights), P, I, F, P, P, P, P, P, P, SZ, P]),
     "wan_profile_begin": (I, [I]),
     "wan_profile_end": (I, [C.POINTER(C.c_char_p), C.POINTER(C.c_double), C.POINTER(C.c_int), I]),
 }
@@ -168,9 +169,9 @@ def wan_attn_workspace_size(B, L, H, d, dtype):
     return lib.wan_attn_workspace_size(B, L, H, d, dtype)
 
 
-def wan_attn_rope3d(q, k, v, o, grid, theta=10000.0, apply_rope=True, ws=None, stream=None):
+def wan_attn_rope3d(q, k, v, o, grid, theta=10000.0, apply_rope=True, ws=None, kv_lens=None, stream=None):
     B, L, H, d = q.shape
-    _check(lib.wan_attn_rope3d(_p(q), _p(k), _p(v), _p(o), B, L, H, d, grid[0], grid[1], grid[2], theta,
+    _check(lib.wan_attn_rope3d(_p(q), _p(k), _p(v), _p(o), _p(kv_lens), B, L, H, d, grid[0], grid[1], grid[2], theta,
                                1 if apply_rope else 0, dtype_code(v.dtype), dtype_code(q.dtype), _p(ws),
                                _nbytes(ws), _stream(stream)), "wan_attn_rope3d")
 
@@ -179,11 +180,12 @@ def wan_cross_attn_workspace_size(B, Lt, Li, H, d, dtype):
     return lib.wan_cross_attn_workspace_size(B, Lt, Li, H, d, dtype)
 
 
-def wan_cross_attn(q, kt, vt, ki, vi, o, ws=None, stream=None):
+def wan_cross_attn(q, kt, vt, ki, vi, o, ws=None, kt_lens=None, stream=None):
     B, L, H, d = q.shape
     Lt = kt.shape[1]
     Li = ki.shape[1] if ki is not None else 0
-    _check(lib.wan_cross_attn(_p(q), _p(kt), _p(vt), _p(ki), _p(vi), _p(o), B, L, Lt, Li, H, d, dtype_code(vt.dtype),
+    _check(lib.wan_cross_attn(_p(q), _p(kt), _p(vt), _p(kt_lens), _p(ki), _p(vi), _p(o), B, L, Lt, Li, H, d,
+                              dtype_code(vt.dtype),
                               dtype_code(q.dtype), _p(ws), _nbytes(ws), _stream(stream)),
            "wan_cross_attn")
 
@@ -242,21 +244,22 @@ def wan_time_embed(cfg, weights, t, e0, hm, t_stride=1, stream=None):
                               ws.numel(), _stream(stream)), "wan_time_embed")
 
 
-def wan_dit_forward(cfg, weights, latent, t, ctx_txt, ctx_img, v_out, ws, latent_broadcast=False, stream=None):
+def wan_dit_forward(cfg, weights, latent, t, ctx_txt, ctx_img, v_out, ws, latent_broadcast=False, txt_lens=None,
+                    stream=None):
     _check(lib.wan_dit_forward(C.byref(cfg), C.byref(weights), _p(latent), 1 if latent_broadcast else 0, _p(t),
-                               _p(ctx_txt), _p(ctx_img), _p(v_out), _p(ws), ws.numel() * ws.element_size(),
+                               _p(ctx_txt), _p(txt_lens), _p(ctx_img), _p(v_out), _p(ws), _nbytes(ws),
                                _stream(stream)), "wan_dit_forward")
 
 
-def wan_dit_guided_step(cfg, weights, x, t_pair, guide_scale, ctx_txt, ctx_img, v_ws, ws, stream=None):
+def wan_dit_guided_step(cfg, weights, x, t_pair, guide_scale, ctx_txt, ctx_img, v_ws, ws, txt_lens=None, stream=None):
     _check(lib.wan_dit_guided_step(C.byref(cfg), C.byref(weights), _p(x), _p(t_pair), guide_scale, _p(ctx_txt),
-                                   _p(ctx_img), _p(v_ws), _p(ws), ws.numel() * ws.element_size(), _stream(stream)),
+                                   _p(txt_lens), _p(ctx_img), _p(v_ws), _p(ws), _nbytes(ws), _stream(stream)),
            "wan_dit_guided_step")
 
 
-def wan_sample(cfg, weights, x, steps, guide_scale, ctx_txt, ctx_img, t_sched, v_ws, ws, stream=None):
-    _check(lib.wan_sample(C.byref(cfg), C.byref(weights), _p(x), steps, guide_scale, _p(ctx_txt), _p(ctx_img),
-                          _p(t_sched), _p(v_ws), _p(ws), ws.numel() * ws.element_size(), _stream(stream)),
+def wan_sample(cfg, weights, x, steps, guide_scale, ctx_txt, ctx_img, t_sched, v_ws, ws, txt_lens=None, stream=None):
+    _check(lib.wan_sample(C.byref(cfg), C.byref(weights), _p(x), steps, guide_scale, _p(ctx_txt), _p(txt_lens),
+                          _p(ctx_img), _p(t_sched), _p(v_ws), _p(ws), _nbytes(ws), _stream(stream)),
            "wan_sample")
 
 
@@ -324,26 +327,28 @@ class DiT:
         wan_time_embed(self.cfg, self.weights_c, t, e0, hm, 1 if t.numel() > 1 else 0, stream)
         return e0, hm
 
-    def forward(self, latent, t, ctx_txt, ctx_img=None, latent_broadcast=False, v_out=None, stream=None):
+    def forward(self, latent, t, ctx_txt, ctx_img=None, latent_broadcast=False, v_out=None, txt_lens=None,
+                stream=None):
         s = self.shape
         if v_out is None:
             v_out = torch.empty(s.batch, s.c_out, s.frames, s.height, s.width, dtype=torch.float32,
                                 device=latent.device)
         wan_dit_forward(self.cfg, self.weights_c, latent, t, ctx_txt, ctx_img, v_out, self.ws, latent_broadcast,
-                        stream)
+                        txt_lens, stream)
         return v_out
 
-    def guided_step(self, x, t_pair, guide_scale, ctx_txt, ctx_img=None, v_ws=None, stream=None):
+    def guided_step(self, x, t_pair, guide_scale, ctx_txt, ctx_img=None, v_ws=None, txt_lens=None, stream=None):
         s = self.shape
         if v_ws is None:
             v_ws = torch.empty(2, s.c_out, s.frames, s.height, s.width, dtype=torch.float32, device=x.device)
         wan_dit_guided_step(self.cfg, self.weights_c, x, t_pair, guide_scale, ctx_txt, ctx_img, v_ws, self.ws,
-                            stream)
+                            txt_lens, stream)
         return v_ws
 
-    def sample(self, x, steps, guide_scale, ctx_txt, ctx_img=None, stream=None):
+    def sample(self, x, steps, guide_scale, ctx_txt, ctx_img=None, txt_lens=None, stream=None):
         s = self.shape
         t_sched = torch.empty(steps + 1, dtype=torch.float32, device=x.device)
         v_ws = torch.empty(2, s.c_out, s.frames, s.height, s.width, dtype=torch.float32, device=x.device)
-        wan_sample(self.cfg, self.weights_c, x, steps, guide_scale, ctx_txt, ctx_img, t_sched, v_ws, self.ws, stream)
+        wan_sample(self.cfg, self.weights_c, x, steps, guide_scale, ctx_txt, ctx_img, t_sched, v_ws, self.ws, txt_lens,
+                   stream)
         return x
