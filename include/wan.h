@@ -280,8 +280,12 @@ int wan_dit_guided_step(const wan_dit_config* cfg, const wan_dit_weights* w, flo
 
 /* [Sampler 3.2, 4.4] End-to-end Euler sampling: `steps` guided steps on the uniform
  * schedule t_k = 1 - k/steps, from noise x (t = 1) to the data estimate (t = 0).
- * t_sched: fp32 DEVICE scratch of steps+1 floats; other arguments as for
- * wan_dit_guided_step. */
+ * The contexts do not depend on t, so every block's cross-attention keys and values are
+ * projected once, into the workspace, and reused by all steps (the same result as
+ * projecting them at every step).  ws: >= wan_sample_workspace_size(cfg) bytes,
+ * 1024-byte aligned.  t_sched: fp32 DEVICE scratch of steps+1 floats; other arguments as
+ * for wan_dit_guided_step. */
+size_t wan_sample_workspace_size(const wan_dit_config* cfg);
 int wan_sample(const wan_dit_config* cfg, const wan_dit_weights* w, float* x, int steps,
                float guide_scale, const void* ctx_txt, const int* txt_lens, const void* ctx_img,
                float* t_sched, float* v_ws, void* ws, size_t ws_bytes, wan_stream_t stream);

@@ -81,6 +81,25 @@ def test_tiny_forward_padded_text(wan, dtype):
         assert_bf16_close(to_np(v), v_o, "v with padded text")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sampler_context_cache_is_exact(wan, dtype):
+    # wan_sample projects the cross-attention keys/values once and reuses them; stepping
+    # by hand with wan_dit_guided_step projects them at every step.  Same arithmetic on
+    # the same operands: the results must agree bit for bit.
+    s = synth.CONFIGS[0].replace(dtype=dtype)
+    w, inp, m = _model(wan, s)
+    ctx = m.text_embed(to_dev(inp["text"], m.tdtype))
+    steps = 3
+    x_a = to_dev(inp["latent"], F32)
+    m.sample(x_a, steps, s.guide_scale, ctx)
+    x_b = to_dev(inp["latent"], F32)
+    ts = torch.tensor(1.0 - np.arange(steps + 1, dtype=np.float32) / steps, device="cuda")
+    for k in range(steps):
+        m.guided_step(x_b, ts[k:k + 2].contiguous(), s.guide_scale, ctx)
+    wan.wan_sync_status()
+    assert torch.equal(x_a, x_b)
+
+
 def test_tiny_forward_batch_permutation(wan):
     # Permuting the batch (latents, timesteps, contexts) permutes the outputs.
     s = synth.CONFIGS[0]

@@ -239,6 +239,15 @@ static FwdWs plan_forward(const wan_dit_config* cfg, void* ws) {
   return w;
 }
 
+// Cross-attention keys/values of every block for a fixed context (the text and image
+// contexts do not depend on t, so a sampler computes them once): per block, text rows
+// [B*Lt, 2D] (k | v) then image rows [B*Li, 2D].
+static size_t ctx_cache_block_bytes(const wan_dit_config* cfg) {
+  const size_t es = cfg->dtype == WAN_F32 ? 4 : 2;
+  return (size_t)round_up((long long)cfg->batch * (cfg->text_len + cfg->img_len) * 2 * cfg->dim * es, 1024);
+}
+static size_t ctx_cache_bytes(const wan_dit_config* cfg) { return ctx_cache_block_bytes(cfg) * cfg->blocks; }
+
 static int validate_cfg(const wan_dit_config* cfg) {
   if (!cfg) return WAN_ERR_INVALID_ARG;
   WAN_TRY(check_dtype(cfg->dtype));
@@ -283,10 +292,33 @@ static int time_embed_impl(const LaunchCtx& c, const wan_dit_config* cfg, const 
   return launch_small_linear(c, e, w->hm_w, w->hm_b, f32, hm, B, 2 * D, D, 1, 0);
 }
 
+// Cross-attention keys/values of block i into kv_txt [B*Lt, 2D] and kv_img [B*Li, 2D].
+static int cross_kv_impl(const LaunchCtx& c, const wan_dit_config* cfg, const wan_block_weights& bw,
+                         const void* ctx_txt, const void* ctx_img, void* kv_txt, void* kv_img) {
+  const int f32 = cfg->dtype == WAN_F32;
+  const int B = cfg->batch, D = cfg->dim;
+  for (int seg = 0; seg < (cfg->img_len ? 2 : 1); ++seg) {
+    const int Lk = seg ? cfg->img_len : cfg->text_len;
+    EpiParams ep = epi_base(EPI_QKV, B * Lk, 2 * D, Lk, seg ? bw.ckvi_b : bw.ckv_b, f32);
+    ep.out = seg ? kv_img : kv_txt;
+    ep.ldo = 2LL * D;
+    ep.out_type = f32 ? OUT_F32 : OUT_BF16;
+    ep.n_rot = 0;
+    ep.n_f16 = f32 ? 0 : D;  // k in fp16, v in bf16
+    ep.head_dim = cfg->head_dim;
+    WAN_TRY(proj(c, f32, seg ? ctx_img : ctx_txt, D, D, seg ? bw.ckvi_w : bw.ckv_w, D, D, B * Lk, 2 * D, D, 0, ep,
+                 "gemm_cross_kv"));
+  }
+  return WAN_OK;
+}
+
+// kv_cache: NULL (each block projects its cross-attention keys/values from the context),
+// or a filled cache of ctx_cache_bytes(cfg) for this context (then no context projection
+// runs).
 static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w, const float* latent,
                             long long lat_bstride, const float* t, int t_stride, const void* ctx_txt,
-                            const int* txt_lens, const void* ctx_img, float* v_out, void* ws, size_t ws_bytes,
-                            cudaStream_t stream) {
+                            const int* txt_lens, const void* ctx_img, const uint8_t* kv_cache, float* v_out,
+                            void* ws, size_t ws_bytes, cudaStream_t stream) {
   WAN_TRY(validate_cfg(cfg));
   WAN_TRY(validate_weights(cfg, w));
   if (!latent || !t || !ctx_txt || !v_out || (cfg->img_len && !ctx_img)) return WAN_ERR_INVALID_ARG;
@@ -365,18 +397,17 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
       ep.out_type = f32 ? OUT_F32 : OUT_F16;
       WAN_TRY(proj(c, f32, W.y, D, D, bw.cq_w, D, D, M, D, D, 0, ep, "gemm_cross_q"));
     }
+    void* kv_txt = W.kvc;
+    void* kv_img = W.kvci;
+    if (kv_cache) {
+      kv_txt = const_cast<uint8_t*>(kv_cache) + (size_t)i * ctx_cache_block_bytes(cfg);
+      kv_img = static_cast<uint8_t*>(kv_txt) + (size_t)B * Lt * 2 * D * (f32 ? 4 : 2);
+    } else {
+      WAN_TRY(cross_kv_impl(c, cfg, bw, ctx_txt, ctx_img, kv_txt, kv_img));
+    }
     for (int seg = 0; seg < (Li ? 2 : 1); ++seg) {
       const int Lk = seg ? Li : Lt;
-      void* kv = seg ? W.kvci : W.kvc;
-      EpiParams ep = epi_base(EPI_QKV, B * Lk, 2 * D, Lk, seg ? bw.ckvi_b : bw.ckv_b, f32);
-      ep.out = kv;
-      ep.ldo = 2LL * D;
-      ep.out_type = f32 ? OUT_F32 : OUT_BF16;
-      ep.n_rot = 0;
-      ep.n_f16 = f32 ? 0 : D;  // k in fp16, v in bf16
-      ep.head_dim = hd;
-      WAN_TRY(proj(c, f32, seg ? ctx_img : ctx_txt, D, D, seg ? bw.ckvi_w : bw.ckv_w, D, D, B * Lk, 2 * D, D, 0, ep,
-                   "gemm_cross_kv"));
+      void* kv = seg ? kv_img : kv_txt;
       AttnArgs a;
       memset(&a, 0, sizeof(a));
       a.q = W.qc; a.ldq = D; a.q_row_len = D; a.q_col = 0;
@@ -724,32 +755,59 @@ int wan_dit_forward(const wan_dit_config* cfg, const wan_dit_weights* w, const f
                     void* ws, size_t ws_bytes, wan_stream_t stream) {
   if (!cfg) return WAN_ERR_INVALID_ARG;
   const long long bstride = latent_broadcast ? 0 : (long long)cfg->c_in * cfg->frames * cfg->height * cfg->width;
-  return dit_forward_impl(cfg, w, latent, bstride, t, 1, ctx_txt, txt_lens, ctx_img, v_out, ws, ws_bytes, stream);
+  return dit_forward_impl(cfg, w, latent, bstride, t, 1, ctx_txt, txt_lens, ctx_img, nullptr, v_out, ws, ws_bytes,
+                          stream);
 }
 
-int wan_dit_guided_step(const wan_dit_config* cfg, const wan_dit_weights* w, float* x, const float* t_pair,
-                        float guide_scale, const void* ctx_txt, const int* txt_lens, const void* ctx_img, float* v_ws,
-                        void* ws, size_t ws_bytes, wan_stream_t stream) {
+static int guided_step_impl(const wan_dit_config* cfg, const wan_dit_weights* w, float* x, const float* t_pair,
+                            float guide_scale, const void* ctx_txt, const int* txt_lens, const void* ctx_img,
+                            const uint8_t* kv_cache, float* v_ws, void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (!cfg || !x || !t_pair || !v_ws) return WAN_ERR_INVALID_ARG;
   if (cfg->batch != 2) return WAN_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(v_ws)) return WAN_ERR_UNSUPPORTED;
-  WAN_TRY(dit_forward_impl(cfg, w, x, 0, t_pair, 0, ctx_txt, txt_lens, ctx_img, v_ws, ws, ws_bytes, stream));
+  WAN_TRY(dit_forward_impl(cfg, w, x, 0, t_pair, 0, ctx_txt, txt_lens, ctx_img, kv_cache, v_ws, ws, ws_bytes, stream));
   LaunchCtx c;
   WAN_TRY(launch_ctx(stream, &c));
   const long long n = (long long)cfg->c_out * cfg->frames * cfg->height * cfg->width;
   return launch_cfg_euler(c, x, v_ws, v_ws + n, n, guide_scale, 0.f, t_pair, 1);
 }
 
+int wan_dit_guided_step(const wan_dit_config* cfg, const wan_dit_weights* w, float* x, const float* t_pair,
+                        float guide_scale, const void* ctx_txt, const int* txt_lens, const void* ctx_img, float* v_ws,
+                        void* ws, size_t ws_bytes, wan_stream_t stream) {
+  return guided_step_impl(cfg, w, x, t_pair, guide_scale, ctx_txt, txt_lens, ctx_img, nullptr, v_ws, ws, ws_bytes,
+                          stream);
+}
+
+size_t wan_sample_workspace_size(const wan_dit_config* cfg) {
+  if (validate_cfg(cfg) != WAN_OK) return 0;
+  return plan_forward(cfg, nullptr).bytes + ctx_cache_bytes(cfg);
+}
+
 int wan_sample(const wan_dit_config* cfg, const wan_dit_weights* w, float* x, int steps, float guide_scale,
                const void* ctx_txt, const int* txt_lens, const void* ctx_img, float* t_sched, float* v_ws, void* ws,
                size_t ws_bytes, wan_stream_t stream) {
   if (!cfg || !x || !t_sched || steps <= 0) return WAN_ERR_INVALID_ARG;
+  WAN_TRY(validate_cfg(cfg));
+  WAN_TRY(validate_weights(cfg, w));
+  if (!ctx_txt || (cfg->img_len && !ctx_img)) return WAN_ERR_INVALID_ARG;
+  const size_t fwd = plan_forward(cfg, nullptr).bytes;
+  if (!ws || ws_bytes < fwd + ctx_cache_bytes(cfg) || (reinterpret_cast<uintptr_t>(ws) & 1023)) return WAN_ERR_WORKSPACE;
   LaunchCtx c;
   WAN_TRY(launch_ctx(stream, &c));
   WAN_TRY(launch_schedule(c, t_sched, steps));
+  // The context is the same for every step: project every block's cross-attention keys
+  // and values once, after the forward workspace, and let every step read them.
+  uint8_t* cache = static_cast<uint8_t*>(ws) + fwd;
+  const size_t es = cfg->dtype == WAN_F32 ? 4 : 2;
+  for (int i = 0; i < cfg->blocks; ++i) {
+    uint8_t* kt = cache + (size_t)i * ctx_cache_block_bytes(cfg);
+    uint8_t* ki = kt + (size_t)cfg->batch * cfg->text_len * 2 * cfg->dim * es;
+    WAN_TRY(cross_kv_impl(c, cfg, w->blocks[i], ctx_txt, ctx_img, kt, ki));
+  }
   for (int k = 0; k < steps; ++k)
-    WAN_TRY(wan_dit_guided_step(cfg, w, x, t_sched + k, guide_scale, ctx_txt, txt_lens, ctx_img, v_ws, ws, ws_bytes,
-                                stream));
+    WAN_TRY(guided_step_impl(cfg, w, x, t_sched + k, guide_scale, ctx_txt, txt_lens, ctx_img, cache, v_ws, ws, fwd,
+                             stream));
   return WAN_OK;
 }
 

@@ -79,6 +79,7 @@ _SIGS = {
     "wan_text_embed_noalloc_max_bytes": (SZ, []),
     "wan_cfg_euler_step": (I, [P, P, P, LL, F, F, I, P]),
     "wan_dit_workspace_size": (SZ, [C.POINTER(wan_dit_config)]),
+    "wan_sample_workspace_size": (SZ, [C.POINTER(wan_dit_config)]),
     "wan_time_embed_workspace_size": (SZ, [C.POINTER(wan_dit_config)]),
     "wan_time_embed": (I, [C.POINTER(wan_dit_config), C.POINTER(wan_dit_weights), P, I, P, P, P, SZ, P]),
     "wan_dit_forward": (I, [C.POINTER(wan_dit_config), C.POINTER(wan_dit_weights), P, I, P, P, P, P, P, P, SZ,
@@ -237,6 +238,10 @@ def wan_dit_workspace_size(cfg: wan_dit_config) -> int:
     return lib.wan_dit_workspace_size(C.byref(cfg))
 
 
+def wan_sample_workspace_size(cfg: wan_dit_config) -> int:
+    return lib.wan_sample_workspace_size(C.byref(cfg))
+
+
 def wan_time_embed(cfg, weights, t, e0, hm, t_stride=1, stream=None):
     ws = torch.empty(lib.wan_time_embed_workspace_size(C.byref(cfg)) + 1024, dtype=torch.uint8, device=t.device)
     ws = ws[(-ws.data_ptr()) % 1024:]
@@ -349,6 +354,9 @@ class DiT:
         s = self.shape
         t_sched = torch.empty(steps + 1, dtype=torch.float32, device=x.device)
         v_ws = torch.empty(2, s.c_out, s.frames, s.height, s.width, dtype=torch.float32, device=x.device)
-        wan_sample(self.cfg, self.weights_c, x, steps, guide_scale, ctx_txt, ctx_img, t_sched, v_ws, self.ws, txt_lens,
-                   stream)
+        n = wan_sample_workspace_size(self.cfg)
+        ws = torch.empty(n + 1024, dtype=torch.uint8, device=x.device)
+        off = (-ws.data_ptr()) % 1024
+        wan_sample(self.cfg, self.weights_c, x, steps, guide_scale, ctx_txt, ctx_img, t_sched, v_ws, ws[off:off + n],
+                   txt_lens, stream)
         return x
