@@ -301,6 +301,7 @@ def run_ours(a, s):
                    "latent": [s.c_in, s.frames, s.height, s.width], "tokens": s.tokens, "dim": s.dim,
                    "heads": s.heads, "head_dim": s.head_dim, "ffn": s.ffn, "text_len": s.text_len,
                    "img_len": s.img_len, "guide_scale": s.guide_scale,
+                   "variant": {"qk_norm": s.qk_norm, "gelu_tanh": s.gelu_tanh},
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: 2.8 GB of weights and ~3 GB of activations stream every step"},
         "tflops": round(tflops, 1), "bf16_peak_frac": round(tflops / pk["bf16_tflops"], 4),
@@ -381,8 +382,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--qk-norm", action="store_true", help="variant: RMSNorm on q and k before RoPE")
+    ap.add_argument("--gelu-tanh", action="store_true", help="variant: tanh-form GELU in the FFN")
     a = ap.parse_args()
-    s = synth.CONFIGS[a.config]
+    s = synth.CONFIGS[a.config].replace(qk_norm=a.qk_norm, gelu_tanh=a.gelu_tanh)
     if a.config in (1, 3):
         s = s.replace(batch=2)  # guided step over a single block: cond + uncond
     if a.impl == "reference":

@@ -66,7 +66,8 @@ enum wan_dtype { WAN_BF16 = 0, WAN_F32 = 1, WAN_F16 = 2 };
 enum wan_epilogue {
   WAN_EPI_STORE = 0,    /* store y in out_dtype */
   WAN_EPI_GELU = 1,     /* store GELU(y) (erf form) in out_dtype */
-  WAN_EPI_RESIDUAL = 2  /* x_f32[m, n] += gate[m / rows_per_gate, n] * y (gate NULL: 1) */
+  WAN_EPI_RESIDUAL = 2, /* x_f32[m, n] += gate[m / rows_per_gate, n] * y (gate NULL: 1) */
+  WAN_EPI_GELU_TANH = 3 /* store GELU(y) in its tanh form, 0.5 y (1 + tanh(sqrt(2/pi)(y + 0.044715 y^3))) */
 };
 
 /* Human-readable text of a status code (static storage). */
@@ -217,6 +218,11 @@ typedef struct wan_dit_config {
   int freq_dim;    /* sinusoid width of the time embedding (256) */
   float theta;     /* RoPE base (10000) */
   float eps;       /* LayerNorm epsilon (1e-6) */
+  /* Variants the pages do not describe, off (0) by default, for fidelity with released
+   * checkpoints: RMSNorm with a learned weight (epsilon eps) on the full-width q and k
+   * before RoPE, and the tanh form of GELU in the FFN. */
+  int qk_norm;
+  int gelu_tanh;
 } wan_dit_config;
 
 typedef struct wan_block_weights {
@@ -229,6 +235,7 @@ typedef struct wan_block_weights {
   const void *co_w, *co_b;          /* [D, D], [D]   cross-attention output */
   const void *f1_w, *f1_b;          /* [F, D], [F] */
   const void *f2_w, *f2_b;          /* [D, F], [D] */
+  const void *norm_q_w, *norm_k_w;  /* [D], [D] RMSNorm weights (only with qk_norm) */
 } wan_block_weights;
 
 typedef struct wan_dit_weights {

@@ -59,6 +59,22 @@ def gelu(x):
     return 0.5 * x * (1.0 + erf(x / np.sqrt(2.0)))
 
 
+def gelu_tanh(x):
+    """The tanh approximation of GELU, 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+    Variant (not on the pages): selected by the gelu_tanh flag for fidelity with released
+    checkpoints that use it."""
+    x = np.asarray(x, f64)
+    return 0.5 * x * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (x + 0.044715 * x ** 3)))
+
+
+def rms_norm(x, w, eps):
+    """RMSNorm over the last axis with a learned weight: x / sqrt(mean(x^2) + eps) * w.
+    Variant (not on the pages): selected by the qk_norm flag, applied to the full width
+    of q and of k before RoPE."""
+    x = np.asarray(x, f64)
+    return x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps) * np.asarray(w, f64)
+
+
 def linear(x, w, b=None):
     """nn.Linear: x [..., in] times w [out, in] transposed, plus bias [out]."""
     y = np.asarray(x, f64) @ np.asarray(w, f64).T
@@ -216,12 +232,14 @@ def heads(x, H):
 class Hyper:
     """The scalars a block needs."""
 
-    def __init__(self, dim, heads, grid, theta=10000.0, eps=1e-6):
+    def __init__(self, dim, heads, grid, theta=10000.0, eps=1e-6, qk_norm=False, gelu_tanh=False):
         self.dim, self.heads, self.grid, self.theta, self.eps = dim, heads, grid, theta, eps
+        self.qk_norm, self.gelu_tanh = qk_norm, gelu_tanh
 
     @classmethod
     def of(cls, shape):
-        return cls(shape.dim, shape.heads, shape.grid, shape.theta, shape.eps)
+        return cls(shape.dim, shape.heads, shape.grid, shape.theta, shape.eps,
+                   getattr(shape, "qk_norm", False), getattr(shape, "gelu_tanh", False))
 
 
 def cross_attention(xr, blk, ctx_txt, ctx_img, hp):
@@ -265,9 +283,12 @@ def dit_block(x, mods, blk, ctx_txt, ctx_img, hp, rows=None, trace=None):
 
     # self-attention with 3D RoPE on q and k [Code, flash_attention call]
     y = modulate(layer_norm(x, hp.eps), sh1, sc1)
-    k = rope3d(heads(linear(y, wk, bk), H), pos, hp.theta)
+    kl, ql = linear(y, wk, bk), linear(y[rows], wq, bq)
+    if hp.qk_norm:  # variant: RMSNorm of the full-width q and k before RoPE
+        kl, ql = rms_norm(kl, blk["norm_k_w"], hp.eps), rms_norm(ql, blk["norm_q_w"], hp.eps)
+    k = rope3d(heads(kl, H), pos, hp.theta)
     v = heads(linear(y, wv, bv), H)
-    q = rope3d(heads(linear(y[rows], wq, bq), H), pos[rows], hp.theta)
+    q = rope3d(heads(ql, H), pos[rows], hp.theta)
     o = attention(q, k, v).reshape(len(rows), D)
     xr = x[rows] + g1 * linear(o, blk["o_w"], blk["o_b"])
     if trace is not None:
@@ -277,7 +298,7 @@ def dit_block(x, mods, blk, ctx_txt, ctx_img, hp, rows=None, trace=None):
     xr = xr + cross_attention(xr, blk, ctx_txt, ctx_img, hp)
 
     y2 = modulate(layer_norm(xr, hp.eps), sh2, sc2)
-    h = gelu(linear(y2, blk["f1_w"], blk["f1_b"]))
+    h = (gelu_tanh if hp.gelu_tanh else gelu)(linear(y2, blk["f1_w"], blk["f1_b"]))
     if trace is not None:
         trace.update(x_ca=xr, y2=y2)
     xr = xr + g2 * linear(h, blk["f2_w"], blk["f2_b"])

@@ -58,6 +58,8 @@ class DiTShape:
     steps: int = 1      # sampling steps (20 for the end-to-end sampler)
     uncond_zero: bool = False   # uncond text embedding = zeros (tiny config)
     i2v: bool = False
+    qk_norm: bool = False       # variant: RMSNorm (learned weight) on q and k before RoPE
+    gelu_tanh: bool = False     # variant: tanh-form GELU in the FFN
 
     @property
     def grid(self):
@@ -161,6 +163,9 @@ def make_weights(s: DiTShape, seed: int = 0) -> dict:
         blk = {}
         for name, shp in block_weight_shapes(s).items():
             blk[name] = store(s, normal(seed, f"block{i}.{name}", shp, WEIGHT_STD))
+        if s.qk_norm:  # RMSNorm weights around 1 (spread so that a mistake in them shows)
+            for name in ("norm_q_w", "norm_k_w"):
+                blk[name] = store(s, 1.0 + normal(seed, f"block{i}.{name}", (s.dim,), 0.1))
         w["blocks"].append(blk)
     return w
 

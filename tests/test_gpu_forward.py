@@ -61,6 +61,25 @@ def test_tiny_guided_step(wan, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dims", [(128, 2, 64), (384, 3, 128)])
+def test_tiny_forward_qk_norm_gelu_tanh_variant(wan, dtype, dims):
+    # The checkpoint-fidelity variant: RMSNorm on q and k before RoPE, tanh-form GELU.
+    D, H, hd = dims
+    s = synth.CONFIGS[0].replace(dtype=dtype, dim=D, heads=H, head_dim=hd, qk_norm=True, gelu_tanh=True)
+    w, inp, m = _model(wan, s)
+    ctx = m.text_embed(to_dev(inp["text"], m.tdtype))
+    lat = np.concatenate([inp["latent"], 0.5 * inp["latent"]], axis=0)
+    t = np.array([0.3, 0.8], np.float32)
+    v = m.forward(to_dev(lat, F32), to_dev(t, F32), ctx)
+    wan.wan_sync_status()
+    v_o = O.dit_forward(lat, t, O.text_projection(inp["text"], w), None, w, s)
+    if dtype == "f32":
+        assert_f32_close(to_np(v), v_o, "v (qk_norm, gelu_tanh)")
+    else:
+        assert_bf16_close(to_np(v), v_o, "v (qk_norm, gelu_tanh)")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_tiny_forward_padded_text(wan, dtype):
     # Padded text contexts with per-entry valid lengths (k_lens of the cross-attention):
     # the result must equal the oracle run on each entry's unpadded context.

@@ -127,6 +127,19 @@ def test_gelu_epilogue_error_bound(wan):
     assert err.max() <= 1e-6, f"GELU epilogue error {err.max():.2e} at x = {x.flat[err.argmax()]}"
 
 
+def test_gelu_tanh_epilogue_error_bound(wan):
+    # The tanh-form GELU variant, x * sigmoid(2u) with SFU exp2 and reciprocal, against its
+    # exact definition: within 1e-6 * max(1, |x|) over [-8, 8].
+    K = 64
+    x = np.linspace(-8.0, 8.0, 512 * K).reshape(512, K).astype(np.float32)
+    w = np.eye(K, dtype=np.float32)
+    out = torch.empty((512, K), dtype=F32, device="cuda")
+    wan.wan_linear(to_dev(x, F32), to_dev(w, F32), None, out, wan.WAN_EPI_GELU_TANH)
+    wan.wan_sync_status()
+    err = np.abs(to_np(out) - O.gelu_tanh(x.astype(np.float64))) / np.maximum(1.0, np.abs(x))
+    assert err.max() <= 1e-6, f"tanh-GELU epilogue error {err.max():.2e} at x = {x.flat[err.argmax()]}"
+
+
 # ---------------------------------------------------------------- self-attention with 3D RoPE
 
 ATTN_CASES = [  # (B, grid, H, d)

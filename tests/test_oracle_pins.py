@@ -374,3 +374,54 @@ def test_latent_geometry_fixture():
         assert [cfg.frames, cfg.height, cfg.width] == lat and cfg.tokens == tokens
     c, s_ = g["i2v_channels"]["c"], g["i2v_channels"]["s"]
     assert 2 * c + s_ == synth.CONFIGS[3].c_in
+
+
+def test_gelu_tanh_variant_textbook_values_and_closeness_to_erf_form():
+    # tanh form = x * sigmoid(odd function of x): exact at 0, GELU(x) - GELU(-x) = x, tends
+    # to x and 0 in the tails, and stays within 1e-3 of the erf form everywhere.
+    assert O.gelu_tanh(0.0) == 0.0
+    x = np.linspace(-6, 6, 1201)
+    assert np.allclose(O.gelu_tanh(x) - O.gelu_tanh(-x), x, atol=1e-14)
+    assert abs(O.gelu_tanh(30.0) - 30.0) < 1e-12 and abs(O.gelu_tanh(-30.0)) < 1e-12
+    assert np.max(np.abs(O.gelu_tanh(x) - O.gelu(x))) < 1e-3
+    # sqrt(2/pi) * (1 + 0.044715) at x = 1: 0.5 (1 + tanh(0.8333...))
+    assert abs(O.gelu_tanh(1.0) - 0.5 * (1.0 + np.tanh(np.sqrt(2 / np.pi) * 1.044715))) < 1e-15
+
+
+def test_rms_norm_variant_unit_rms_scale_invariance_and_weight():
+    rng = np.random.default_rng(3)
+    x = rng.normal(size=(7, 64)) * 3.0
+    ones = np.ones(64)
+    y = O.rms_norm(x, ones, 0.0)
+    assert np.allclose(np.sqrt((y ** 2).mean(axis=-1)), 1.0, atol=1e-13)
+    assert np.allclose(O.rms_norm(5.0 * x, ones, 0.0), y, atol=1e-13)       # invariant to a positive scale
+    assert np.allclose(O.rms_norm(-x, ones, 0.0), -y, atol=1e-13)           # odd
+    w = rng.normal(size=64)
+    assert np.allclose(O.rms_norm(x, w, 0.0), y * w, atol=1e-13)           # weight is elementwise
+    # eps: a zero row stays zero; a tiny row is damped, not blown up
+    assert np.all(O.rms_norm(np.zeros((1, 64)), ones, 1e-6) == 0.0)
+
+
+def test_qk_norm_variant_makes_block_invariant_to_q_k_projection_scale():
+    # With RMSNorm on q and k, scaling the q and k projection weights and biases by any
+    # positive factor leaves the block unchanged (the norm removes the scale; only the
+    # eps = 1e-6 term, ~1e-5 of mean(q^2) here, is not scaled).
+    s = synth.CONFIGS[0].replace(qk_norm=True, gelu_tanh=True)
+    w = synth.make_weights(s, 0)
+    inp = synth.make_inputs(s, 0)
+    hp = O.Hyper.of(s)
+    x = O.patchify(inp["latent"], w["patch_w"], w["patch_b"])[0]
+    ctx = O.text_projection(inp["text"][:1], w)[0]
+    mods = np.zeros((6, s.dim)) + 0.1
+    blk = w["blocks"][0]
+    base = O.dit_block(x, mods, blk, ctx, None, hp)
+    blk2 = dict(blk)
+    D = s.dim
+    blk2["qkv_w"] = blk["qkv_w"].copy(); blk2["qkv_b"] = blk["qkv_b"].copy()
+    blk2["qkv_w"][:2 * D] *= 7.5
+    blk2["qkv_b"][:2 * D] *= 7.5
+    assert np.allclose(O.dit_block(x, mods, blk2, ctx, None, hp), base, rtol=1e-4, atol=1e-6)
+    # ... while without the norm the same scaling changes the result
+    hp_plain = O.Hyper.of(s.replace(qk_norm=False))
+    assert not np.allclose(O.dit_block(x, mods, blk2, ctx, None, hp_plain),
+                           O.dit_block(x, mods, blk, ctx, None, hp_plain), rtol=1e-3, atol=1e-3)

@@ -276,6 +276,8 @@ static int validate_weights(const wan_dit_config* cfg, const wan_dit_weights* w)
     for (const void* p : q)
       if (!p || !aligned16(p)) return WAN_ERR_INVALID_ARG;
     if (cfg->img_len && (!b.ckvi_w || !b.ckvi_b)) return WAN_ERR_INVALID_ARG;
+    if (cfg->qk_norm && (!b.norm_q_w || !b.norm_k_w || !aligned16(b.norm_q_w) || !aligned16(b.norm_k_w)))
+      return WAN_ERR_INVALID_ARG;
   }
   return WAN_OK;
 }
@@ -361,11 +363,13 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
       ep.out = W.qkv;
       ep.ldo = 3LL * D;
       ep.out_type = f32 ? OUT_F32 : OUT_BF16;
-      ep.n_rot = 2 * D;
-      ep.n_f16 = f32 ? 0 : 2 * D;  // q, k feed the QK^T MMA in fp16
+      ep.n_rot = cfg->qk_norm ? 0 : 2 * D;  // with q/k RMSNorm, RoPE follows the norm below
+      ep.n_f16 = f32 ? 0 : 2 * D;           // q, k feed the QK^T MMA in fp16
       ep.head_dim = hd;
       ep.rope = rg;
       WAN_TRY(proj(c, f32, W.y, D, D, bw.qkv_w, D, D, M, 3 * D, D, 0, ep, "gemm_qkv_rope"));
+      if (cfg->qk_norm)
+        WAN_TRY(launch_qk_rmsnorm_rope(c, W.qkv, 3LL * D, bw.norm_q_w, bw.norm_k_w, rg, M, L, D, hd, cfg->eps, f32));
     }
     {
       AttnArgs a;
@@ -431,7 +435,7 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
     // --- FFN: y = LN(x)(1+sc2)+sh2; h = GELU(y W1^T + b1); x += g2 (h W2^T + b2)
     WAN_TRY(launch_ln_mod(c, W.x, mod + 3 * D, mod + 4 * D, 6LL * D, W.y, f32, M, L, D, cfg->eps));
     {
-      EpiParams ep = epi_base(EPI_GELU, M, Fh, L, bw.f1_b, f32);
+      EpiParams ep = epi_base(cfg->gelu_tanh ? EPI_GELU_TANH : EPI_GELU, M, Fh, L, bw.f1_b, f32);
       ep.out = W.h;
       ep.ldo = Fh;
       ep.out_type = f32 ? OUT_F32 : OUT_BF16;
@@ -654,7 +658,9 @@ int wan_linear(const void* x, const void* w, const void* b, void* out, int M, in
   if (out_dtype != WAN_BF16 && out_dtype != WAN_F32 && out_dtype != WAN_F16) return WAN_ERR_INVALID_ARG;
   const int f32 = dtype == WAN_F32;
   if (!x || !w || !out || M <= 0 || N <= 0 || K <= 0) return WAN_ERR_INVALID_ARG;
-  if (epilogue != WAN_EPI_STORE && epilogue != WAN_EPI_GELU && epilogue != WAN_EPI_RESIDUAL) return WAN_ERR_INVALID_ARG;
+  if (epilogue != WAN_EPI_STORE && epilogue != WAN_EPI_GELU && epilogue != WAN_EPI_RESIDUAL &&
+      epilogue != WAN_EPI_GELU_TANH)
+    return WAN_ERR_INVALID_ARG;
   if (gate && rows_per_gate <= 0) return WAN_ERR_INVALID_ARG;
   if (f32 && out_dtype != WAN_F32) return WAN_ERR_UNSUPPORTED;
   if (epilogue == WAN_EPI_RESIDUAL && out_dtype != WAN_F32) return WAN_ERR_UNSUPPORTED;
@@ -663,7 +669,10 @@ int wan_linear(const void* x, const void* w, const void* b, void* out, int M, in
     return WAN_ERR_UNSUPPORTED;
   LaunchCtx c;
   WAN_TRY(launch_ctx(stream, &c));
-  const int kind = epilogue == WAN_EPI_STORE ? EPI_STORE : (epilogue == WAN_EPI_GELU ? EPI_GELU : EPI_RESID);
+  const int kind = epilogue == WAN_EPI_STORE ? EPI_STORE
+                   : epilogue == WAN_EPI_GELU ? EPI_GELU
+                   : epilogue == WAN_EPI_GELU_TANH ? EPI_GELU_TANH
+                                                   : EPI_RESID;
   EpiParams ep = epi_base(kind, M, N, gate ? rows_per_gate : M, b, f32);
   if (kind == EPI_RESID) {
     ep.resid = static_cast<float*>(out);

@@ -414,4 +414,76 @@ int launch_watchdog_selftest(const LaunchCtx& c, unsigned long long limit_ns) {
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------ q/k RMSNorm + RoPE (variant)
+// One 128-thread CTA per token row of the q | k | v buffer: for q (columns [0, D)) and k
+// ([D, 2D)): x <- RoPE(x * rsqrt(mean(x^2) + eps) * w), in place, fp32 statistics.
+template <typename T>
+__device__ __forceinline__ float2 ld2(const T* p) {
+  if constexpr (sizeof(T) == 4) return make_float2(p[0], p[1]);
+  else return __half22float2(*reinterpret_cast<const __half2*>(p));
+}
+template <typename T>
+__device__ __forceinline__ void st2(T* p, float2 v) {
+  if constexpr (sizeof(T) == 4) { p[0] = v.x; p[1] = v.y; }
+  else *reinterpret_cast<__half2*>(p) = __floats2half2_rn(v.x, v.y);
+}
+
+template <typename T, typename WT>
+__global__ void __launch_bounds__(128) qk_rmsnorm_rope_kernel(T* __restrict__ qkv, long long ld, const WT* __restrict__ wq,
+                                                              const WT* __restrict__ wk, RopeGeom g, int L, int D,
+                                                              int hd, float eps) {
+  __shared__ float red[2][4];
+  const long long row = blockIdx.x;
+  const int l = (int)(row % L);
+  const int t = threadIdx.x;
+  T* base = qkv + row * ld;
+  float s[2] = {0.f, 0.f};
+  for (int part = 0; part < 2; ++part)
+    for (int c = 2 * t; c < D; c += 256) {
+      const float2 v = ld2(base + part * D + c);
+      s[part] += v.x * v.x + v.y * v.y;
+    }
+#pragma unroll
+  for (int part = 0; part < 2; ++part) {
+    float a = s[part];
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    if ((t & 31) == 0) red[part][t >> 5] = a;
+  }
+  __syncthreads();
+  float r[2];
+#pragma unroll
+  for (int part = 0; part < 2; ++part)
+    r[part] = rsqrtf(((red[part][0] + red[part][1]) + (red[part][2] + red[part][3])) / (float)D + eps);
+  for (int part = 0; part < 2; ++part) {
+    const WT* w = part ? wk : wq;
+    for (int c = 2 * t; c < D; c += 256) {
+      float2 v = ld2(base + part * D + c);
+      float x[2];
+      if constexpr (sizeof(WT) == 4) {
+        x[0] = v.x * r[part] * w[c];
+        x[1] = v.y * r[part] * w[c + 1];
+      } else {
+        x[0] = v.x * r[part] * bf2f(w[c]);
+        x[1] = v.y * r[part] * bf2f(w[c + 1]);
+      }
+      epi_rope<2>(g, hd, c % hd, l, x);
+      st2(base + part * D + c, make_float2(x[0], x[1]));
+    }
+  }
+}
+
+int launch_qk_rmsnorm_rope(const LaunchCtx& c, void* qkv, long long ld, const void* wq, const void* wk, const RopeGeom& g,
+                           int rows, int L, int D, int hd, float eps, int f32) {
+  if (rows <= 0) return WAN_OK;
+  count_launch("qk_rmsnorm_rope", c.stream, true);
+  if (f32)
+    qk_rmsnorm_rope_kernel<float, float><<<rows, 128, 0, c.stream>>>(
+        static_cast<float*>(qkv), ld, static_cast<const float*>(wq), static_cast<const float*>(wk), g, L, D, hd, eps);
+  else
+    qk_rmsnorm_rope_kernel<__half, bf16><<<rows, 128, 0, c.stream>>>(
+        static_cast<__half*>(qkv), ld, static_cast<const bf16*>(wq), static_cast<const bf16*>(wk), g, L, D, hd, eps);
+  count_launch("qk_rmsnorm_rope", c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
 }  // namespace wan

@@ -16,6 +16,7 @@ enum EpiKind : int {
   EPI_RESID = 2,  // resid[m, n] += gate[b, n] * (acc + bias)   (gate NULL: 1)
   EPI_QKV = 3,    // out[m, n] = acc + bias, RoPE on cols [0, n_rot), fp16 on cols [0, n_f16)
   EPI_HEAD = 4,   // depatchify: vout[b, c, f, 2i+di, 2j+dj] = acc + bias, n = c*4 + di*2 + dj
+  EPI_GELU_TANH = 5,  // out[m, n] = GELU_tanh(acc + bias)
 };
 
 struct RopeGeom {
@@ -185,6 +186,11 @@ __device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int m, int n0
   const int b = m / p.rows_per_batch;
   const int l = m - b * p.rows_per_batch;
   switch (p.kind) {
+    case EPI_GELU_TANH:
+#pragma unroll
+      for (int i = 0; i < CNT; ++i) v[i] = gelu_tanh_form(v[i]);
+      epi_store_row<CNT>(p.out, p.out_type, (long long)m * p.ldo + n0, v);
+      break;
     case EPI_GELU:
 #pragma unroll
       for (int i = 0; i < CNT; ++i) v[i] = gelu_erf(v[i]);

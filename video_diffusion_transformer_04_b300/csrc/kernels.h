@@ -72,6 +72,9 @@ int launch_block_mods(const LaunchCtx& c, const float* e0, const void* const* mo
 int launch_rope_apply(const LaunchCtx& c, const void* in, void* out, const RopeGeom& g, int B, int L, int H, int d,
                       int in_type);
 int launch_schedule(const LaunchCtx& c, float* ts, int steps);
+// In place on the q | k | v rows (row stride ld): q and k <- RoPE(RMSNorm(.) * w) over D.
+int launch_qk_rmsnorm_rope(const LaunchCtx& c, void* qkv, long long ld, const void* wq, const void* wk,
+                           const RopeGeom& g, int rows, int L, int D, int hd, float eps, int f32);
 // A kernel whose only wait never completes: it gives up after limit_ns (status word set).
 int launch_watchdog_selftest(const LaunchCtx& c, unsigned long long limit_ns);
 

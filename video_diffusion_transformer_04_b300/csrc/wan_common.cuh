@@ -381,6 +381,15 @@ __device__ __forceinline__ float erf_as7126(float z) {
   return copysignf(fmaf(-poly, e, 1.0f), z);
 }
 
+// Tanh form of GELU: 0.5 x (1 + tanh(u)) = x * sigmoid(2u), u = sqrt(2/pi) (x + 0.044715 x^3),
+// evaluated as x / (1 + 2^(-2u log2 e)) with SFU exp2 and reciprocal (relative error ~1e-6).
+__device__ __forceinline__ float gelu_tanh_form(float x) {
+  const float u2 = 1.5957691216057308f * fmaf(0.044715f * x, x * x, x);  // 2u
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(1.0f + ex2_approx(-u2 * 1.4426950408889634f)));
+  return x * r;
+}
+
 __device__ __forceinline__ float gelu_erf(float x) {
   return 0.5f * x * (1.0f + erf_as7126(x * 0.70710678118654752440f));
 }

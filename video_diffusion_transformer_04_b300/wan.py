@@ -18,7 +18,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libwan.so"
 
 WAN_OK, WAN_ERR_INVALID_ARG, WAN_ERR_UNSUPPORTED, WAN_ERR_CUDA, WAN_ERR_TIMEOUT, WAN_ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
 WAN_BF16, WAN_F32, WAN_F16 = 0, 1, 2
-WAN_EPI_STORE, WAN_EPI_GELU, WAN_EPI_RESIDUAL = 0, 1, 2
+WAN_EPI_STORE, WAN_EPI_GELU, WAN_EPI_RESIDUAL, WAN_EPI_GELU_TANH = 0, 1, 2, 3
 
 
 class WanError(RuntimeError):
@@ -42,11 +42,11 @@ P, I, LL, F, SZ = C.c_void_p, C.c_int, C.c_longlong, C.c_float, C.c_size_t
 class wan_dit_config(C.Structure):
     _fields_ = [("dtype", I), ("batch", I), ("c_in", I), ("c_out", I), ("frames", I), ("height", I), ("width", I),
                 ("dim", I), ("heads", I), ("head_dim", I), ("ffn", I), ("blocks", I), ("text_len", I),
-                ("img_len", I), ("freq_dim", I), ("theta", F), ("eps", F)]
+                ("img_len", I), ("freq_dim", I), ("theta", F), ("eps", F), ("qk_norm", I), ("gelu_tanh", I)]
 
 
 _BLOCK_FIELDS = ["mod", "qkv_w", "qkv_b", "o_w", "o_b", "cq_w", "cq_b", "ckv_w", "ckv_b", "ckvi_w", "ckvi_b",
-                 "co_w", "co_b", "f1_w", "f1_b", "f2_w", "f2_b"]
+                 "co_w", "co_b", "f1_w", "f1_b", "f2_w", "f2_b", "norm_q_w", "norm_k_w"]
 _GLOBAL_FIELDS = ["patch_w", "patch_b", "t1_w", "t1_b", "t2_w", "t2_b", "m_w", "m_b", "hm_w", "hm_b", "head_w",
                   "head_b"]
 
@@ -299,7 +299,8 @@ class DiT:
             c_out=shape.c_out, frames=shape.frames, height=shape.height, width=shape.width, dim=shape.dim,
             heads=shape.heads, head_dim=shape.head_dim, ffn=shape.ffn, blocks=shape.blocks,
             text_len=shape.text_len, img_len=shape.img_len, freq_dim=shape.freq_dim, theta=shape.theta,
-            eps=shape.eps)
+            eps=shape.eps, qk_norm=int(getattr(shape, "qk_norm", False)),
+            gelu_tanh=int(getattr(shape, "gelu_tanh", False)))
         up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=self.tdtype)
         self.tensors = {k: up(v) for k, v in weights.items() if k != "blocks"}
         self.block_tensors = [{k: up(v) for k, v in blk.items()} for blk in weights["blocks"]]
