@@ -1,7 +1,8 @@
 #!/usr/bin/env python
 """Benchmark of the Wan DiT guided denoising step on B300 (libwan, sm_103a).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 2]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload wan1.3b-30blk-guided-step | wan1.3b-block | wan14b-i2v-block]
 
 One step = one pass of the whole hot path over the 30-block 1.3B-shaped DiT at 480p
 (21x60x104 latent -> 32760 tokens), batch 2 (cond + uncond): text projection, time
@@ -297,7 +298,7 @@ def run_ours(a, s):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": round(ms / a.steps, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) latent and text, N(0,0.02) weights)",
-        "config": {"workload": f"config {a.config}: {s.name}", "blocks": s.blocks, "batch": s.batch,
+        "config": {"workload": s.name, "blocks": s.blocks, "batch": s.batch,
                    "latent": [s.c_in, s.frames, s.height, s.width], "tokens": s.tokens, "dim": s.dim,
                    "heads": s.heads, "head_dim": s.head_dim, "ffn": s.ffn, "text_len": s.text_len,
                    "img_len": s.img_len, "guide_scale": s.guide_scale,
@@ -366,7 +367,7 @@ def run_reference(a, s):
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1,
            "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(step_s * 1e3, 1), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": f"config {a.config}: {s.name}", "tokens": s.tokens, "blocks": s.blocks,
+           "config": {"workload": s.name, "tokens": s.tokens, "blocks": s.blocks,
                       "batch": s.batch},
            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
                             "sample": sample},
@@ -380,13 +381,14 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3])
+    ap.add_argument("--workload", default="wan1.3b-30blk-guided-step",
+                    choices=["wan1.3b-30blk-guided-step", "wan1.3b-block", "wan14b-i2v-block"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--qk-norm", action="store_true", help="variant: RMSNorm on q and k before RoPE")
     ap.add_argument("--gelu-tanh", action="store_true", help="variant: tanh-form GELU in the FFN")
     a = ap.parse_args()
-    s = synth.CONFIGS[a.config].replace(qk_norm=a.qk_norm, gelu_tanh=a.gelu_tanh)
-    if a.config in (1, 3):
+    s = synth.WORKLOADS[a.workload].replace(qk_norm=a.qk_norm, gelu_tanh=a.gelu_tanh)
+    if s.blocks == 1:
         s = s.replace(batch=2)  # guided step over a single block: cond + uncond
     if a.impl == "reference":
         run_reference(a, s)

@@ -74,17 +74,26 @@ class DiTShape:
         return dataclasses.replace(self, **kw)
 
 
-# The five workloads of the benchmark description (0-based).
-CONFIGS = {
-    0: DiTShape("tiny-f32", "f32", 2, 16, 16, 3, 8, 8, 128, 2, 64, 512, 1, 16, 128,
-                uncond_zero=True),
-    1: DiTShape("wan1.3b-block", "bf16", 1, 16, 16, 21, 60, 104, 1536, 12, 128, 8960, 1, 512, 4096),
-    2: DiTShape("wan1.3b-30blk-guided-step", "bf16", 2, 16, 16, 21, 60, 104, 1536, 12, 128, 8960, 30, 512, 4096),
-    3: DiTShape("wan14b-i2v-block", "bf16", 1, 36, 16, 21, 90, 160, 5120, 40, 128, 13824, 1, 512, 0,
-                img_len=257, i2v=True),
-    4: DiTShape("wan1.3b-20step-sampler", "bf16", 2, 16, 16, 21, 60, 104, 1536, 12, 128, 8960, 30, 512, 4096,
-                steps=20),
-}
+# The workloads, by name:
+#   tiny-f32                   one block, fp32, 16x3x8x8 latent -> 48 tokens, D=128, 2 heads of 64
+#   wan1.3b-block              one 1.3B-shaped block, bf16, 480p latent 16x21x60x104 -> 32760 tokens
+#   wan1.3b-30blk-guided-step  the 30-block 1.3B-shaped DiT, one guided step (cond + uncond)
+#   wan14b-i2v-block           one 14B-shaped I2V block, 720p latent 36x21x90x160 -> 75600 tokens
+#   wan1.3b-20step-sampler     the 30-block DiT, 20 guided Euler steps
+WORKLOADS = {s.name: s for s in (
+    DiTShape("tiny-f32", "f32", 2, 16, 16, 3, 8, 8, 128, 2, 64, 512, 1, 16, 128, uncond_zero=True),
+    DiTShape("wan1.3b-block", "bf16", 1, 16, 16, 21, 60, 104, 1536, 12, 128, 8960, 1, 512, 4096),
+    DiTShape("wan1.3b-30blk-guided-step", "bf16", 2, 16, 16, 21, 60, 104, 1536, 12, 128, 8960, 30, 512, 4096),
+    DiTShape("wan14b-i2v-block", "bf16", 1, 36, 16, 21, 90, 160, 5120, 40, 128, 13824, 1, 512, 0,
+             img_len=257, i2v=True),
+    DiTShape("wan1.3b-20step-sampler", "bf16", 2, 16, 16, 21, 60, 104, 1536, 12, 128, 8960, 30, 512, 4096,
+             steps=20),
+)}
+TINY = WORKLOADS["tiny-f32"]
+BLOCK_1P3B = WORKLOADS["wan1.3b-block"]
+STEP_1P3B = WORKLOADS["wan1.3b-30blk-guided-step"]
+BLOCK_14B_I2V = WORKLOADS["wan14b-i2v-block"]
+SAMPLER_1P3B = WORKLOADS["wan1.3b-20step-sampler"]
 
 
 def _gen(seed: int, name: str) -> np.random.Generator:

@@ -5,12 +5,13 @@ from the seeded synthetic inputs (``synth``); nothing comes from the CUDA path.
 The GPU tests regenerate the same inputs from the same seeds and compare the
 kernels' outputs with these values at the stored positions.
 
-    python tests/golden/make_goldens.py --config 1     # one 1.3B block (minutes)
-    python tests/golden/make_goldens.py --config 2     # 30 blocks x 2 branches (~30 min on 8 cores)
-    python tests/golden/make_goldens.py --config 3     # one 14B I2V block
-    python tests/golden/make_goldens.py --config 4     # 20-step sampler on a shrunk latent
+    python tests/golden/make_goldens.py --workload wan1.3b-block               # one 1.3B block (minutes)
+    python tests/golden/make_goldens.py --workload wan1.3b-30blk-guided-step   # 30 blocks x 2 branches (~3 h on 8 cores)
+    python tests/golden/make_goldens.py --workload wan14b-i2v-block            # one 14B I2V block
+    python tests/golden/make_goldens.py --workload wan1.3b-20step-sampler      # 20 steps on a shrunk latent
 
-Outputs ``tests/golden/config<N>.npz`` (float32 values, int64 indices).
+Outputs ``tests/golden/<workload>.npz`` (``-shrunk`` for the sampler; float32 values,
+int64 indices).
 """
 import argparse
 import os
@@ -35,8 +36,8 @@ def f32(a):
     return np.asarray(a, np.float32)
 
 
-def single_block(cfg_id, n_rows):
-    s = synth.CONFIGS[cfg_id]
+def single_block(name, n_rows):
+    s = synth.WORKLOADS[name]
     w = synth.make_weights(s, SEED)
     inp = synth.make_inputs(s, SEED)
     if s.text_dim:
@@ -60,7 +61,7 @@ def single_block(cfg_id, n_rows):
 
 
 def guided_step_full(n_rows):
-    s = synth.CONFIGS[2]
+    s = synth.STEP_1P3B
     w = synth.make_weights(s, SEED)
     inp = synth.make_inputs(s, SEED)
     ctx = O.text_projection(inp["text"], w)
@@ -76,7 +77,7 @@ def guided_step_full(n_rows):
 
 
 def sampler_shrunk():
-    s = synth.CONFIGS[4].replace(**SHRUNK_SAMPLER)
+    s = synth.SAMPLER_1P3B.replace(**SHRUNK_SAMPLER)
     w = synth.make_weights(s, SEED)
     inp = synth.make_inputs(s, SEED)
     ctx = O.text_projection(inp["text"], w)
@@ -86,18 +87,21 @@ def sampler_shrunk():
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--config", type=int, required=True, choices=[1, 2, 3, 4])
+    ap.add_argument("--workload", required=True, choices=["wan1.3b-block", "wan1.3b-30blk-guided-step",
+                                                          "wan14b-i2v-block", "wan1.3b-20step-sampler"])
     a = ap.parse_args()
     t0 = time.time()
-    if a.config == 1:
-        out = single_block(1, 512)
-    elif a.config == 3:
-        out = single_block(3, 256)
-    elif a.config == 2:
+    name = a.workload
+    if name == "wan1.3b-block":
+        out = single_block(name, 512)
+    elif name == "wan14b-i2v-block":
+        out = single_block(name, 256)
+    elif name == "wan1.3b-30blk-guided-step":
         out = guided_step_full(512)
     else:
         out = sampler_shrunk()
-    path = os.path.join(HERE, f"config{a.config}.npz")
+        name += "-shrunk"
+    path = os.path.join(HERE, f"{name}.npz")
     np.savez_compressed(path, **out)
     print(f"wrote {path} in {time.time() - t0:.1f} s")
 

@@ -83,7 +83,7 @@ def test_host_validation_rejects_bad_arguments(wanlib):
 def test_dit_workspace_size_arithmetic():
     import synth
     from video_diffusion_transformer_04_b300 import wan
-    s = synth.CONFIGS[2]
+    s = synth.STEP_1P3B
     cfg = wan.wan_dit_config(dtype=wan.WAN_BF16, batch=2, c_in=16, c_out=16, frames=21, height=60, width=104,
                              dim=1536, heads=12, head_dim=128, ffn=8960, blocks=30, text_len=512, img_len=0,
                              freq_dim=256, theta=10000.0, eps=1e-6)

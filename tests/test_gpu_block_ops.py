@@ -1,7 +1,7 @@
 """One DiT block composed from the per-op entry points (wan_patchify, wan_time_embed,
 wan_adaln_modulate, wan_linear, wan_attn_rope3d, wan_cross_attn, wan_ffn) at the
 full 1.3B and 14B block sizes, checked after every sub-layer against the oracle's
-intermediates stored at sampled rows (tests/golden/config{1,3}.npz)."""
+intermediates stored at sampled rows (tests/golden/wan1.3b-block.npz, wan14b-i2v-block.npz)."""
 import os
 
 import numpy as np
@@ -16,13 +16,13 @@ BF, F16, F32 = torch.bfloat16, torch.float16, torch.float32
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
-@pytest.mark.parametrize("n", [1, 3])
-def test_block_composed_from_ops(wan, n):
-    path = os.path.join(GOLDEN, f"config{n}.npz")
+@pytest.mark.parametrize("name", ["wan1.3b-block", "wan14b-i2v-block"])
+def test_block_composed_from_ops(wan, name):
+    path = os.path.join(GOLDEN, f"{name}.npz")
     if not os.path.exists(path):
         pytest.skip("golden not generated")
     g = np.load(path)
-    s = synth.CONFIGS[n]
+    s = synth.WORKLOADS[name]
     w = synth.make_weights(s, 0)
     inp = synth.make_inputs(s, 0)
     m = wan.DiT(s, w)
@@ -32,8 +32,8 @@ def test_block_composed_from_ops(wan, n):
     rows = g["rows"][:len(g["x0"])]
     dev = "cuda"
 
-    def check(name, tensor):
-        assert_bf16_close(to_np(tensor)[0, rows], g[name], f"config {n} {name}")
+    def check(key, tensor):
+        assert_bf16_close(to_np(tensor)[0, rows], g[key], f"{name} {key}")
 
     lat = to_dev(inp["latent"], F32)
     x = torch.empty(1, L, D, dtype=F32, device=dev)

@@ -27,8 +27,8 @@ def _model(wan, s, seed=0):
     return w, inp, wan.DiT(s, w)
 
 
-def _golden(n):
-    path = os.path.join(GOLDEN, f"config{n}.npz")
+def _golden(name):
+    path = os.path.join(GOLDEN, f"{name}.npz")
     if not os.path.exists(path):
         pytest.skip(f"{path} not generated")
     return np.load(path)
@@ -36,7 +36,7 @@ def _golden(n):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_tiny_guided_step(wan, dtype):
-    s = synth.CONFIGS[0].replace(dtype=dtype)
+    s = synth.TINY.replace(dtype=dtype)
     w, inp, m = _model(wan, s)
     tdt = m.tdtype
     ctx = m.text_embed(to_dev(inp["text"], tdt))
@@ -65,7 +65,7 @@ def test_tiny_guided_step(wan, dtype):
 def test_tiny_forward_qk_norm_gelu_tanh_variant(wan, dtype, dims):
     # The checkpoint-fidelity variant: RMSNorm on q and k before RoPE, tanh-form GELU.
     D, H, hd = dims
-    s = synth.CONFIGS[0].replace(dtype=dtype, dim=D, heads=H, head_dim=hd, qk_norm=True, gelu_tanh=True)
+    s = synth.TINY.replace(dtype=dtype, dim=D, heads=H, head_dim=hd, qk_norm=True, gelu_tanh=True)
     w, inp, m = _model(wan, s)
     ctx = m.text_embed(to_dev(inp["text"], m.tdtype))
     lat = np.concatenate([inp["latent"], 0.5 * inp["latent"]], axis=0)
@@ -83,7 +83,7 @@ def test_tiny_forward_qk_norm_gelu_tanh_variant(wan, dtype, dims):
 def test_tiny_forward_padded_text(wan, dtype):
     # Padded text contexts with per-entry valid lengths (k_lens of the cross-attention):
     # the result must equal the oracle run on each entry's unpadded context.
-    s = synth.CONFIGS[0].replace(dtype=dtype)
+    s = synth.TINY.replace(dtype=dtype)
     w, inp, m = _model(wan, s)
     tdt = m.tdtype
     ctx = m.text_embed(to_dev(inp["text"], tdt))
@@ -105,7 +105,7 @@ def test_sampler_context_cache_is_exact(wan, dtype):
     # wan_sample projects the cross-attention keys/values once and reuses them; stepping
     # by hand with wan_dit_guided_step projects them at every step.  Same arithmetic on
     # the same operands: the results must agree bit for bit.
-    s = synth.CONFIGS[0].replace(dtype=dtype)
+    s = synth.TINY.replace(dtype=dtype)
     w, inp, m = _model(wan, s)
     ctx = m.text_embed(to_dev(inp["text"], m.tdtype))
     steps = 3
@@ -121,7 +121,7 @@ def test_sampler_context_cache_is_exact(wan, dtype):
 
 def test_tiny_forward_batch_permutation(wan):
     # Permuting the batch (latents, timesteps, contexts) permutes the outputs.
-    s = synth.CONFIGS[0]
+    s = synth.TINY
     w, inp, m = _model(wan, s)
     ctx = m.text_embed(to_dev(inp["text"], F32))
     lat = torch.cat([to_dev(inp["latent"], F32), 0.5 * to_dev(inp["latent"], F32)])
@@ -132,9 +132,9 @@ def test_tiny_forward_batch_permutation(wan):
     assert_f32_close(to_np(v2), to_np(v1)[::-1], "permuted batch", tol=1e-6)
 
 
-def _check_single_block(wan, n):
-    g = _golden(n)
-    s = synth.CONFIGS[n]
+def _check_single_block(wan, name):
+    g = _golden(name)
+    s = synth.WORKLOADS[name]
     w, inp, m = _model(wan, s)
     if s.text_dim:
         ctx = m.text_embed(to_dev(inp["text"], BF))
@@ -145,20 +145,20 @@ def _check_single_block(wan, n):
     v = m.forward(to_dev(inp["latent"], F32), to_dev(inp["t"], F32), ctx, ctx_img)
     wan.wan_sync_status()
     head = tokens_of(to_np(v))[0, g["rows"]]
-    assert_bf16_close(head, g["head"], f"config {n} head rows")
+    assert_bf16_close(head, g["head"], f"{name} head rows")
 
 
-def test_config1_block(wan):
-    _check_single_block(wan, 1)
+def test_wan13b_block(wan):
+    _check_single_block(wan, "wan1.3b-block")
 
 
-def test_config3_i2v_block(wan):
-    _check_single_block(wan, 3)
+def test_wan14b_i2v_block(wan):
+    _check_single_block(wan, "wan14b-i2v-block")
 
 
-def test_config2_guided_step(wan):
-    g = _golden(2)
-    s = synth.CONFIGS[2]
+def test_wan13b_30blk_guided_step(wan):
+    g = _golden("wan1.3b-30blk-guided-step")
+    s = synth.STEP_1P3B
     w, inp, m = _model(wan, s)
     del w
     ctx = m.text_embed(to_dev(inp["text"], BF))
@@ -174,10 +174,10 @@ def test_config2_guided_step(wan):
     assert_bf16_close(tokens_of(to_np(x))[0, rows], g["x_next"], "x_next")
 
 
-def test_config4_sampler_shrunk(wan):
-    g = _golden(4)
+def test_wan13b_20step_sampler_shrunk(wan):
+    g = _golden("wan1.3b-20step-sampler-shrunk")
     Fr, H, W = (int(a) for a in g["shape"])
-    s = synth.CONFIGS[4].replace(frames=Fr, height=H, width=W)
+    s = synth.SAMPLER_1P3B.replace(frames=Fr, height=H, width=W)
     w, inp, m = _model(wan, s)
     del w
     ctx = m.text_embed(to_dev(inp["text"], BF))

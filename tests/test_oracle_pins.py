@@ -278,7 +278,7 @@ def test_euler_zero_velocity_and_cfg_euler():
 # ---------------------------------------------------------------- block / forward
 
 def _tiny(seed=0, **kw):
-    s = synth.CONFIGS[0].replace(**kw)
+    s = synth.TINY.replace(**kw)
     w = synth.make_weights(s, seed)
     inp = synth.make_inputs(s, seed)
     return s, w, inp
@@ -370,10 +370,10 @@ def test_latent_geometry_fixture():
         assert lat == case["latent"]
         tokens = lat[0] * (lat[1] // 2) * (lat[2] // 2)
         assert tokens == case["tokens"]
-        cfg = synth.CONFIGS[case["config"]]
+        cfg = synth.WORKLOADS[case["workload"]]
         assert [cfg.frames, cfg.height, cfg.width] == lat and cfg.tokens == tokens
     c, s_ = g["i2v_channels"]["c"], g["i2v_channels"]["s"]
-    assert 2 * c + s_ == synth.CONFIGS[3].c_in
+    assert 2 * c + s_ == synth.BLOCK_14B_I2V.c_in
 
 
 def test_gelu_tanh_variant_textbook_values_and_closeness_to_erf_form():
@@ -406,7 +406,7 @@ def test_qk_norm_variant_makes_block_invariant_to_q_k_projection_scale():
     # With RMSNorm on q and k, scaling the q and k projection weights and biases by any
     # positive factor leaves the block unchanged (the norm removes the scale; only the
     # eps = 1e-6 term, ~1e-5 of mean(q^2) here, is not scaled).
-    s = synth.CONFIGS[0].replace(qk_norm=True, gelu_tanh=True)
+    s = synth.TINY.replace(qk_norm=True, gelu_tanh=True)
     w = synth.make_weights(s, 0)
     inp = synth.make_inputs(s, 0)
     hp = O.Hyper.of(s)
