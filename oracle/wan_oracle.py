@@ -222,6 +222,155 @@ def attention(q, k, v, chunk=2048):
     return out
 
 
+# ---------------------------------------------------------------- 8-bit variant
+# [Method] hyper.ai summary, section 方法 (Method), the inference paragraph: FP8 GEMMs and
+# an 8-bit FlashAttention speed up the DiT.  The pages fix neither the 8-bit format nor
+# the scaling; READING (the plainest one that the hardware runs natively): OCP FP8 E4M3
+# codes, round to nearest even with saturation at +-448, each tensor scaled by its
+# absolute maximum over a group so that the maximum maps to 448:
+#   GEMM activations per row (token), GEMM weights per output channel;
+#   attention q per (token, head), k per (head, 128-key block), v per (head, channel).
+# The quantisation decisions are taken in fp32, like the kernels: inv = fl32(448 / amax),
+# code = e4m3(fl32(x * inv)), dequantisation scale s = fl32(amax / 448) (0 when amax = 0).
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(code):
+    """Value of an E4M3 code (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+    infinities; exponent 15 with mantissa 7 is NaN; exponent 0 holds the subnormals
+    M * 2^-9)."""
+    c = np.asarray(code, np.int64) & 0xFF
+    sgn = np.where(c & 0x80, -1.0, 1.0)
+    E, M = (c >> 3) & 0xF, c & 7
+    val = np.where(E == 0, M * 2.0 ** -9, (1.0 + M / 8.0) * 2.0 ** (E.astype(f64) - 7.0))
+    val = np.where((E == 15) & (M == 7), np.nan, val)
+    return sgn * val
+
+
+def e4m3_round(x):
+    """Nearest E4M3 value to x (ties to even), magnitudes above 448 saturated to 448.
+    The grid spacing in the binade [2^e, 2^(e+1)) is 2^(e-3) for e >= -6 and 2^-9 below."""
+    x = np.asarray(x, f64)
+    a = np.abs(x)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))          # a = m 2^ex, m in [0.5, 1)
+    e = np.maximum(ex.astype(f64) - 1.0, -6.0)         # floor(log2 a), floored at -6
+    ulp = 2.0 ** (e - 3.0)
+    r = np.minimum(np.rint(a / ulp) * ulp, E4M3_MAX)   # a / ulp is exact: rint = ties-to-even
+    return np.where(a > 0, np.sign(x) * r, 0.0 * x)
+
+
+def e4m3_encode(x):
+    """E4M3 code of e4m3_round(x) (the byte the kernels store)."""
+    r = e4m3_round(x)
+    a = np.abs(r)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    e = ex.astype(np.int64) - 1
+    normal = a >= 2.0 ** -6
+    mant_n = np.rint((a / np.ldexp(1.0, e) - 1.0) * 8.0).astype(np.int64)
+    code_n = ((e + 7) << 3) | mant_n
+    code_s = np.rint(a / 2.0 ** -9).astype(np.int64)
+    code = np.where(normal, code_n, code_s)
+    return (code | np.where(np.signbit(r), 0x80, 0)).astype(np.uint8)
+
+
+def _f32(x):
+    return np.asarray(x, np.float32)
+
+
+def quant_scale(amax):
+    """(inv, s) for a group absolute maximum: inv = fl32(448 / amax) multiplies the values
+    before rounding, s = fl32(amax / 448) dequantises.  An all-zero group gets inv = s = 0."""
+    amax = _f32(amax)
+    safe = np.where(amax > 0, amax, np.float32(1))
+    inv = np.where(amax > 0, np.float32(E4M3_MAX) / safe, np.float32(0)).astype(np.float32)
+    s = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    return inv, s
+
+
+def quantize_groups(x, axes):
+    """Codes and dequantisation scales of x with one scale per group; ``axes`` are the
+    axes each group spans (reduced by the absolute maximum).  x is taken as fp32."""
+    x32 = _f32(x)
+    amax = np.abs(x32).max(axis=axes, keepdims=True)
+    inv, s = quant_scale(amax)
+    codes = e4m3_encode((x32 * inv).astype(np.float32))
+    return codes, s
+
+
+def quant_rows(x):
+    """Per-row E4M3 quantisation of a [rows, K] matrix: codes [rows, K], scales [rows]."""
+    c, s = quantize_groups(x, axes=(-1,))
+    return c, s[..., 0]
+
+
+def dequant(codes, s):
+    return e4m3_decode(codes) * np.asarray(s, f64)
+
+
+def linear_fp8(a_codes, sa, w_codes, sw, b=None):
+    """FP8 GEMM: (A8 sa) (W8 sw)^T + b, every product exact, accumulation in fp64.
+    a_codes [M, K] with row scales sa [M]; w_codes [N, K] with per-output-channel scales
+    sw [N]."""
+    y = (e4m3_decode(a_codes) @ e4m3_decode(w_codes).T) * np.asarray(sa, f64)[:, None] * np.asarray(sw, f64)[None, :]
+    if b is not None:
+        y = y + np.asarray(b, f64)
+    return y
+
+
+def quant_attn_q(q):
+    """q [L, H, d] -> codes [L, H, d], scales [L, H] (one per token and head)."""
+    c, s = quantize_groups(q, axes=(-1,))
+    return c, s[..., 0]
+
+
+def quant_attn_k(k, block=128):
+    """k [L, H, d] -> codes [L, H, d], scales [H, ceil(L/block)] (one per head and block
+    of ``block`` consecutive keys; a ragged last block spans the keys it has)."""
+    k32 = _f32(k)
+    L, H, d = k32.shape
+    nb = (L + block - 1) // block
+    codes = np.empty(k32.shape, np.uint8)
+    scales = np.empty((H, nb), np.float32)
+    for j in range(nb):
+        c, s = quantize_groups(k32[j * block:(j + 1) * block], axes=(0, 2))
+        codes[j * block:(j + 1) * block] = c
+        scales[:, j] = s[0, :, 0]
+    return codes, scales
+
+
+def quant_attn_v(v):
+    """v [L, H, d] -> codes [L, H, d], scales [H, d] (one per head and channel, over all
+    keys)."""
+    c, s = quantize_groups(v, axes=(0,))
+    return c, s[0]
+
+
+def attention_8bit(q8, sq, k8, sk, v8, sv, block=128, kv_len=None):
+    """Attention on the dequantised 8-bit operands, softmax and products in fp64:
+    softmax(Q K^T / sqrt(d)) V with Q = dec(q8) sq, K = dec(k8) sk (per key block),
+    V = dec(v8) sv; only the first kv_len keys take part.  The kernel's own rounding of
+    the probabilities to E4M3 is not modelled here: its effect is bounded by
+    2^-4 * attention(q, k, |V|) per element (relative error of E4M3 rounding in the
+    normal range), which the parity tests use."""
+    Q = dequant(q8, np.asarray(sq)[..., None])
+    blk_of_key = np.arange(k8.shape[0]) // block
+    K = e4m3_decode(k8) * np.asarray(sk, f64).T[blk_of_key][:, :, None]
+    V = e4m3_decode(v8) * np.asarray(sv, f64)[None]
+    if kv_len is not None:
+        K, V = K[:kv_len], V[:kv_len]
+    return attention(Q, K, V)
+
+
+def self_attention_8bit(q, k, v, kv_len=None):
+    """The 8-bit self-attention of the variant: quantise q, k, v as above, then
+    attention_8bit.  Returns (o, (Q, K, V) dequantised) for bound computations."""
+    q8, sq = quant_attn_q(q)
+    k8, sk = quant_attn_k(k)
+    v8, sv = quant_attn_v(v)
+    return attention_8bit(q8, sq, k8, sk, v8, sv, kv_len=kv_len)
+
+
 def heads(x, H):
     x = np.asarray(x, f64)
     return x.reshape(x.shape[0], H, x.shape[1] // H)
@@ -232,14 +381,16 @@ def heads(x, H):
 class Hyper:
     """The scalars a block needs."""
 
-    def __init__(self, dim, heads, grid, theta=10000.0, eps=1e-6, qk_norm=False, gelu_tanh=False):
+    def __init__(self, dim, heads, grid, theta=10000.0, eps=1e-6, qk_norm=False, gelu_tanh=False, fp8=0):
         self.dim, self.heads, self.grid, self.theta, self.eps = dim, heads, grid, theta, eps
         self.qk_norm, self.gelu_tanh = qk_norm, gelu_tanh
+        self.fp8 = fp8  # bit 0: 8-bit self-attention; bit 1: FP8 QKV and FFN-up GEMMs
 
     @classmethod
     def of(cls, shape):
         return cls(shape.dim, shape.heads, shape.grid, shape.theta, shape.eps,
-                   getattr(shape, "qk_norm", False), getattr(shape, "gelu_tanh", False))
+                   getattr(shape, "qk_norm", False), getattr(shape, "gelu_tanh", False),
+                   getattr(shape, "fp8", 0))
 
 
 def cross_attention(xr, blk, ctx_txt, ctx_img, hp):
@@ -283,13 +434,24 @@ def dit_block(x, mods, blk, ctx_txt, ctx_img, hp, rows=None, trace=None):
 
     # self-attention with 3D RoPE on q and k [Code, flash_attention call]
     y = modulate(layer_norm(x, hp.eps), sh1, sc1)
-    kl, ql = linear(y, wk, bk), linear(y[rows], wq, bq)
+    if hp.fp8 & 2:  # variant: FP8 GEMM, activations per token, weights per output channel
+        y8, sy = quant_rows(y)
+        wq8, swq = quant_rows(wq)
+        wk8, swk = quant_rows(wk)
+        wv8, swv = quant_rows(wv)
+        kl, ql = linear_fp8(y8, sy, wk8, swk, bk), linear_fp8(y8[rows], sy[rows], wq8, swq, bq)
+        vl = linear_fp8(y8, sy, wv8, swv, bv)
+    else:
+        kl, ql, vl = linear(y, wk, bk), linear(y[rows], wq, bq), linear(y, wv, bv)
     if hp.qk_norm:  # variant: RMSNorm of the full-width q and k before RoPE
         kl, ql = rms_norm(kl, blk["norm_k_w"], hp.eps), rms_norm(ql, blk["norm_q_w"], hp.eps)
     k = rope3d(heads(kl, H), pos, hp.theta)
-    v = heads(linear(y, wv, bv), H)
+    v = heads(vl, H)
     q = rope3d(heads(ql, H), pos[rows], hp.theta)
-    o = attention(q, k, v).reshape(len(rows), D)
+    if hp.fp8 & 1:  # variant: 8-bit self-attention
+        o = self_attention_8bit(q, k, v).reshape(len(rows), D)
+    else:
+        o = attention(q, k, v).reshape(len(rows), D)
     xr = x[rows] + g1 * linear(o, blk["o_w"], blk["o_b"])
     if trace is not None:
         trace.update(y1=y[rows], q=q.reshape(len(rows), D), k=k[rows].reshape(len(rows), D),
@@ -298,7 +460,13 @@ def dit_block(x, mods, blk, ctx_txt, ctx_img, hp, rows=None, trace=None):
     xr = xr + cross_attention(xr, blk, ctx_txt, ctx_img, hp)
 
     y2 = modulate(layer_norm(xr, hp.eps), sh2, sc2)
-    h = (gelu_tanh if hp.gelu_tanh else gelu)(linear(y2, blk["f1_w"], blk["f1_b"]))
+    if hp.fp8 & 2:
+        y28, sy2 = quant_rows(y2)
+        w18, sw1 = quant_rows(blk["f1_w"])
+        u = linear_fp8(y28, sy2, w18, sw1, blk["f1_b"])
+    else:
+        u = linear(y2, blk["f1_w"], blk["f1_b"])
+    h = (gelu_tanh if hp.gelu_tanh else gelu)(u)
     if trace is not None:
         trace.update(x_ca=xr, y2=y2)
     xr = xr + g2 * linear(h, blk["f2_w"], blk["f2_b"])

@@ -60,6 +60,7 @@ class DiTShape:
     i2v: bool = False
     qk_norm: bool = False       # variant: RMSNorm (learned weight) on q and k before RoPE
     gelu_tanh: bool = False     # variant: tanh-form GELU in the FFN
+    fp8: int = 0                # variant bits: 1 = 8-bit self-attention, 2 = FP8 QKV / FFN-up GEMMs
 
     @property
     def grid(self):

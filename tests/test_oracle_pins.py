@@ -425,3 +425,213 @@ def test_qk_norm_variant_makes_block_invariant_to_q_k_projection_scale():
     hp_plain = O.Hyper.of(s.replace(qk_norm=False))
     assert not np.allclose(O.dit_block(x, mods, blk2, ctx, None, hp_plain),
                            O.dit_block(x, mods, blk, ctx, None, hp_plain), rtol=1e-3, atol=1e-3)
+
+
+# ---------------------------------------------------------------- 8-bit variant
+
+def _grid_values(shape, r):
+    """Random finite E4M3 values (codes 0x00..0x7E with random sign) scaled by 2^r."""
+    codes = rng.integers(0, 0x7F, size=shape)
+    sign = np.where(rng.random(shape) < 0.5, -1.0, 1.0)
+    return O.e4m3_decode(codes) * sign * np.ldexp(1.0, r)
+
+
+def test_e4m3_decode_format_values():
+    # OCP 8-bit floating point, E4M3: bias 7, max normal 1.75 * 2^8 = 448, min normal 2^-6,
+    # min subnormal 2^-9, S.1111.111 is NaN, no infinities.
+    v = O.e4m3_decode(np.arange(256))
+    assert v[0x7E] == 448.0 and v[0xFE] == -448.0
+    assert v[0x08] == 2.0 ** -6 and v[0x07] == 7 * 2.0 ** -9 and v[0x01] == 2.0 ** -9
+    assert v[0x38] == 1.0 and v[0x39] == 1.125 and v[0x40] == 2.0 and v[0x30] == 0.5
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and np.isnan(v).sum() == 2
+    pos = v[1:0x7F]
+    assert len(pos) == 126 and np.all(np.diff(pos) > 0)
+    # the library's E4M3 ("fn": finite + NaN) type decodes the same bytes the same way
+    import torch
+    tv = torch.from_numpy(np.arange(256, dtype=np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+    fin = ~np.isnan(v)
+    assert np.array_equal(tv[fin], v[fin]) and np.all(np.isnan(tv[~fin]))
+
+
+def test_e4m3_round_ties_to_even_saturation_and_library_agreement():
+    import torch
+    x = (rng.standard_normal(200000) * np.exp(rng.uniform(-12, 6, 200000))).astype(np.float32)
+    x = x[np.abs(x) < 448]
+    lib = torch.from_numpy(x).to(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(O.e4m3_round(x), lib)
+    # midpoints between neighbours round to the even mantissa
+    v = O.e4m3_decode(np.arange(0, 0x7E))
+    mids = 0.5 * (v[:-1] + v[1:])
+    r = O.e4m3_round(mids)
+    even = np.where(np.arange(0, 0x7D) % 2 == 0, v[:-1], v[1:])
+    assert np.array_equal(r, even)
+    # saturation at +-448 (the kernels' satfinite conversion), identity on the grid
+    assert np.array_equal(O.e4m3_round([449.0, 464.0, 1e9, -1e9]), [448.0, 448.0, 448.0, -448.0])
+    fin = np.concatenate([v, -v])
+    assert np.array_equal(O.e4m3_round(fin), fin)
+    codes = np.arange(256)
+    ok = ~np.isnan(O.e4m3_decode(codes))
+    assert np.array_equal(O.e4m3_encode(O.e4m3_decode(codes[ok])), codes[ok].astype(np.uint8))
+
+
+def test_quant_rows_max_maps_to_448_and_error_bound():
+    x = rng.standard_normal((64, 300)) * np.exp(rng.uniform(-8, 8, (64, 1)))
+    x[3] = 0.0
+    codes, s = O.quant_rows(x)
+    x32 = x.astype(np.float32).astype(np.float64)
+    i = np.abs(x32).argmax(axis=1)
+    rows = np.arange(64) != 3
+    assert np.all(np.abs(O.e4m3_decode(codes[np.arange(64), i]))[rows] == 448.0)
+    assert np.all(codes[3] == 0) and s[3] == 0.0
+    d = O.dequant(codes, s[:, None])
+    err = np.abs(d - x32)
+    normal = np.abs(x32) >= (2.0 ** -6) * s[:, None] * 1.0001
+    # relative 2^-4 (half an ulp of 3 mantissa bits) in the normal range, 2^-10 s below,
+    # plus the fp32 rounding of the scaled value
+    assert np.all(err[normal] <= (2.0 ** -4 + 1e-6) * np.abs(x32[normal]))
+    assert np.all(err[~normal] <= (2.0 ** -10 + 1e-6) * np.broadcast_to(s[:, None], err.shape)[~normal])
+
+
+def test_linear_fp8_exact_on_representable_inputs_and_brute_force():
+    # Each row of A (and of W) holds E4M3 grid values times 2^r with one entry equal to
+    # 448 * 2^r: its scale is 2^r exactly and quantisation is the identity, so the FP8
+    # GEMM must equal the exact product (checked by plain loops on a small case).
+    M, N, K = 5, 4, 9
+    ra, rw = rng.integers(-6, 6, M), rng.integers(-6, 6, N)
+    A = np.stack([_grid_values(K, r) for r in ra]); A[np.arange(M), rng.integers(0, K, M)] = 448.0 * np.ldexp(1.0, ra)
+    W = np.stack([_grid_values(K, r) for r in rw]); W[np.arange(N), rng.integers(0, K, N)] = -448.0 * np.ldexp(1.0, rw)
+    a8, sa = O.quant_rows(A)
+    w8, sw = O.quant_rows(W)
+    assert np.array_equal(sa, np.ldexp(1.0, ra)) and np.array_equal(sw, np.ldexp(1.0, rw))
+    b = rng.standard_normal(N)
+    y = O.linear_fp8(a8, sa, w8, sw, b)
+    for m in range(M):
+        for n in range(N):
+            acc = b[n]
+            for k in range(K):
+                acc += A[m, k] * W[n, k]
+            assert y[m, n] == pytest.approx(acc, rel=1e-13, abs=1e-12)
+
+
+def test_linear_fp8_scales_are_per_row_and_per_channel():
+    # Rows and channels of very different magnitudes keep the E4M3 relative accuracy;
+    # one scale per tensor would flush the small ones to zero.
+    A = rng.standard_normal((8, 256)) * np.array([1e-4, 1, 1e3, 1, 1e-2, 1, 30, 1])[:, None]
+    W = rng.standard_normal((6, 256)) * np.array([1e-3, 1, 1e2, 1, 1, 5e-2])[:, None]
+    a8, sa = O.quant_rows(A)
+    w8, sw = O.quant_rows(W)
+    y = O.linear_fp8(a8, sa, w8, sw)
+    ref = A @ W.T
+    # each product carries at most (1 + 2^-4)^2 - 1 relative error
+    bound = (2 * 2.0 ** -4 + 2.0 ** -8) * (np.abs(A) @ np.abs(W).T)
+    assert np.all(np.abs(y - ref) <= bound)
+    # error relative to sum |a w|: ~2^-4 / sqrt(K) for independent roundings, on every row
+    # (a per-tensor activation scale measures 0.13-0.23 on the 1e-4 row)
+    rel = np.abs(y - ref) / (np.abs(A) @ np.abs(W).T)
+    assert rel.max() < 0.04 and np.median(rel) < 0.006
+
+
+def _attn_operands(L, H, d, block=128):
+    """q, k, v on scaled E4M3 grids whose group maxima are 448 * 2^r exactly."""
+    q = np.empty((L, H, d)); k = np.empty((L, H, d)); v = np.empty((L, H, d))
+    for l in range(L):
+        for h in range(H):
+            r = int(rng.integers(-7, -3))
+            q[l, h] = _grid_values(d, r); q[l, h, rng.integers(0, d)] = 448.0 * 2.0 ** r
+    for h in range(H):
+        for j0 in range(0, L, block):
+            r = int(rng.integers(-7, -3))
+            n = min(block, L - j0)
+            k[j0:j0 + n, h] = _grid_values((n, d), r)
+            k[j0 + rng.integers(0, n), h, rng.integers(0, d)] = -448.0 * 2.0 ** r
+        for c in range(d):
+            r = int(rng.integers(-5, 3))
+            v[:, h, c] = _grid_values(L, r); v[rng.integers(0, L), h, c] = 448.0 * 2.0 ** r
+    return q, k, v
+
+
+def test_attention_8bit_exact_on_representable_inputs():
+    # Quantisation is the identity on these operands, so the 8-bit attention equals the
+    # exact attention; a scale applied along the wrong axis (per key instead of per key
+    # block, per token instead of per channel for v) or a dropped one breaks the equality.
+    L, H, d = 300, 2, 16
+    q, k, v = _attn_operands(L, H, d)
+    q8, sq = O.quant_attn_q(q)
+    k8, sk = O.quant_attn_k(k)
+    v8, sv = O.quant_attn_v(v)
+    assert sq.shape == (L, H) and sk.shape == (H, 3) and sv.shape == (H, d)
+    assert np.array_equal(O.dequant(q8, sq[..., None]), q)
+    o8 = O.attention_8bit(q8, sq, k8, sk, v8, sv)
+    assert np.allclose(o8, O.attention(q, k, v), rtol=1e-12, atol=1e-14 * np.abs(v).max())
+    # key masking: only the first kv_len keys; with one key every row returns v[0]
+    o1 = O.attention_8bit(q8, sq, k8, sk, v8, sv, kv_len=1)
+    assert np.allclose(o1, np.broadcast_to(v[0], o1.shape), rtol=1e-14, atol=0)
+    o_m = O.attention_8bit(q8, sq, k8, sk, v8, sv, kv_len=200)
+    assert np.allclose(o_m, O.attention(q, k[:200], v[:200]), rtol=1e-12, atol=1e-14 * np.abs(v).max())
+
+
+def test_attention_quantisers_group_by_token_head_key_block_and_channel():
+    # Brute force over the groups: each scale is the group's |max| / 448 and every value of
+    # the group keeps E4M3 relative accuracy, whatever the other groups' magnitudes.
+    L, H, d, blk = 300, 2, 8, 128
+    mag = np.exp(rng.uniform(-10, 10, (L, H, d)))
+    x = rng.standard_normal((L, H, d)) * mag
+    x32 = x.astype(np.float32).astype(np.float64)
+    q8, sq = O.quant_attn_q(x)
+    k8, sk = O.quant_attn_k(x, blk)
+    v8, sv = O.quant_attn_v(x)
+
+    def check(codes, scale_of):
+        err = np.abs(O.e4m3_decode(codes) * scale_of - x32)
+        normal = np.abs(x32) >= 2.0 ** -6 * scale_of * 1.0001
+        assert np.all(err[normal] <= (2.0 ** -4 + 1e-6) * np.abs(x32[normal]))
+        assert np.all(err[~normal] <= (2.0 ** -10 + 1e-6) * scale_of[~normal])
+
+    sq_b, sk_b, sv_b = np.empty((L, H, d)), np.empty((L, H, d)), np.empty((L, H, d))
+    for h in range(H):
+        for l in range(L):
+            assert sq[l, h] == np.float32(np.abs(x32[l, h]).max() / np.float32(448))
+            sq_b[l, h] = sq[l, h]
+        for j in range(3):
+            g = x32[j * blk:(j + 1) * blk, h]
+            assert sk[h, j] == np.float32(np.abs(g).max() / np.float32(448))
+            sk_b[j * blk:(j + 1) * blk, h] = sk[h, j]
+        for c in range(d):
+            assert sv[h, c] == np.float32(np.abs(x32[:, h, c]).max() / np.float32(448))
+            sv_b[:, h, c] = sv[h, c]
+    check(q8, sq_b)
+    check(k8, sk_b)
+    check(v8, sv_b)
+
+
+def test_attention_8bit_channel_scales_keep_relative_accuracy():
+    # Value channels of very different magnitudes: every output channel keeps E4M3
+    # relative accuracy (one scale per tensor would zero the small channels).
+    L, H, d = 384, 1, 32
+    q = rng.standard_normal((L, H, d))
+    k = rng.standard_normal((L, H, d)) * np.repeat([0.3, 1.0, 2.0], 128)[:, None, None]
+    v = rng.standard_normal((L, H, d)) * np.exp(rng.uniform(-9, 9, d))[None, None, :]
+    o8 = O.self_attention_8bit(q, k, v)
+    ref = O.attention(q, k, v)
+    rel = np.abs(o8 - ref) / np.abs(O.attention(q, k, np.abs(v)))
+    assert rel.max() < 0.25 and np.median(rel) < 0.05
+
+
+def test_fp8_block_variant_close_to_exact_and_zero_gates_reduce_to_exact():
+    s = synth.TINY
+    w = synth.make_weights(s, 0)
+    inp = synth.make_inputs(s, 0)
+    x = O.patchify(inp["latent"], w["patch_w"], w["patch_b"])[0]
+    ctx = O.text_projection(inp["text"][:1], w)[0]
+    blk = w["blocks"][0]
+    mods = np.zeros((6, s.dim)) + 0.1
+    exact = O.dit_block(x, mods, blk, ctx, None, O.Hyper.of(s))
+    for bits in (1, 2, 3):
+        y = O.dit_block(x, mods, blk, ctx, None, O.Hyper.of(s.replace(fp8=bits)))
+        d = (y - x) - (exact - x)
+        rel = np.sqrt((d ** 2).mean() / ((exact - x) ** 2).mean())
+        assert 1e-4 < rel < 0.08, (bits, rel)
+    # gates 0: self-attention and FFN contribute nothing, only cross-attention (not 8-bit)
+    mods0 = mods.copy(); mods0[2] = 0.0; mods0[5] = 0.0
+    y0 = O.dit_block(x, mods0, blk, ctx, None, O.Hyper.of(s.replace(fp8=3)))
+    assert np.allclose(y0, O.dit_block(x, mods0, blk, ctx, None, O.Hyper.of(s)), rtol=0, atol=1e-12)
