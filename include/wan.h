@@ -166,6 +166,50 @@ int wan_linear(const void* x, const void* w, const void* b, void* out, int M, in
                int epilogue, const float* gate, int rows_per_gate, int dtype, int out_dtype,
                wan_stream_t stream);
 
+/* ------------------------------------------------------------------ 8-bit variant
+ * [Method] (hyper.ai summary of the Wan report, section 方法, the inference paragraph):
+ * FP8 GEMMs and an 8-bit FlashAttention speed up the DiT.  READING (the pages fix no
+ * format or scaling): OCP FP8 E4M3 codes, round to nearest even, saturating at +-448;
+ * one scale per group, decided in fp32: amax = max |x|, inv = 448 / amax,
+ * code = e4m3(x * inv), dequantisation scale s = amax / 448 (an all-zero group: s = 0).
+ * Groups: GEMM activations per row (token), GEMM weights per row (output channel);
+ * attention q per (token, head), k per (head, block of 128 keys), v per (head, channel)
+ * over all keys.  Codes are plain bytes (no device type in these signatures).
+ *
+ * wan_quant_rows_e4m3: x [M, K] in dtype (WAN_BF16, WAN_F16 or WAN_F32; row stride ldx
+ *   elements, 16-byte aligned rows) -> x8 [M, K] codes (row stride ld8 bytes), s [M] fp32.
+ *   K, ldx and ld8 multiples of 4. */
+int wan_quant_rows_e4m3(const void* x, int dtype, long long ldx, int M, int K, void* x8, long long ld8,
+                        float* s, wan_stream_t stream);
+
+/* wan_quant_attn_e4m3: the 8-bit operands of self-attention.
+ *   q, k: [B, L, H*d] in qk_dtype; v: [B, L, H*d] in v_dtype (WAN_BF16 or WAN_F16 each).
+ *   Outputs (device, caller-owned): q8 [B, L, H*d] codes, sq [B, L, H];
+ *   k8 [B, L, H*d], sk [B, H, ceil(L/128)]; v8t [B, H, d, Lp] (v transposed, keys
+ *   contiguous, Lp = L rounded up to 16, pad keys zero), sv [B, H, d].
+ *   ws: >= wan_quant_attn_workspace_size(B, H, d) bytes (per-channel |max| of v).
+ *   d must be 128; all pointers 16-byte aligned. */
+size_t wan_quant_attn_workspace_size(int B, int H, int d);
+int wan_quant_attn_e4m3(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int B, int L,
+                        int H, int d, void* q8, float* sq, void* k8, float* sk, void* v8t, float* sv,
+                        void* ws, size_t ws_bytes, wan_stream_t stream);
+
+/* wan_attn_e4m3: o = softmax(Q K^T / sqrt(d)) V with Q, K, V the dequantised operands in
+ *   the layouts wan_quant_attn_e4m3 writes; both products run on 8-bit tensor cores with
+ *   fp32 accumulation, the probabilities are rounded to E4M3 inside the kernel (relative
+ *   error <= 2^-4 each in the normal range).  o: bf16 [B, L, H*d]; kv_lens as for
+ *   wan_attn_rope3d.  d must be 128. */
+int wan_attn_e4m3(const void* q8, const float* sq, const void* k8, const float* sk, const void* v8t,
+                  const float* sv, void* o, const int* kv_lens, int B, int L, int H, int d, wan_stream_t stream);
+
+/* wan_linear_e4m3: out = (x8 sx)(w8 sw)^T + b, every product of two codes exact, fp32
+ *   accumulation, with an epilogue as for wan_linear: WAN_EPI_STORE / WAN_EPI_GELU /
+ *   WAN_EPI_GELU_TANH write bf16 out [M, N]; WAN_EPI_RESIDUAL accumulates into fp32 out
+ *   with the optional gate.  x8 [M, K] codes, sx [M]; w8 [N, K] codes, sw [N] (16-byte
+ *   aligned); b [N] bf16 or NULL.  K % 16 == 0, N % 32 == 0. */
+int wan_linear_e4m3(const void* x8, const float* sx, const void* w8, const float* sw, const void* b, void* out,
+                    int M, int N, int K, int epilogue, const float* gate, int rows_per_gate, wan_stream_t stream);
+
 /* ------------------------------------------------------------------ text projection
  * Projection of the text-encoder output (umT5 width Ct) to the DiT width D.
  * READING (pages silent on its form): ctx = W2 GELU(W1 text + b1) + b2.
@@ -223,6 +267,11 @@ typedef struct wan_dit_config {
    * before RoPE, and the tanh form of GELU in the FFN. */
   int qk_norm;
   int gelu_tanh;
+  /* 8-bit variant (bf16 path, head_dim 128), off (0) by default: bit 0 = 8-bit
+   * self-attention, bit 1 = FP8 QKV and FFN-up GEMMs (their activations leave the
+   * LayerNorm + modulation pass as per-token E4M3 codes; the weights come quantised per
+   * output channel in wan_block_weights). */
+  int fp8;
 } wan_dit_config;
 
 typedef struct wan_block_weights {
@@ -236,6 +285,12 @@ typedef struct wan_block_weights {
   const void *f1_w, *f1_b;          /* [F, D], [F] */
   const void *f2_w, *f2_b;          /* [D, F], [D] */
   const void *norm_q_w, *norm_k_w;  /* [D], [D] RMSNorm weights (only with qk_norm) */
+  /* only with fp8 bit 1: E4M3 codes of qkv_w and f1_w and their per-row scales, as
+   * written by wan_quant_rows_e4m3 */
+  const void* qkv_w8;
+  const float* qkv_ws;              /* [3D] */
+  const void* f1_w8;
+  const float* f1_ws;               /* [F] */
 } wan_block_weights;
 
 typedef struct wan_dit_weights {

@@ -9,9 +9,10 @@ kernels' outputs with these values at the stored positions.
     python tests/golden/make_goldens.py --workload wan1.3b-30blk-guided-step   # 30 blocks x 2 branches (~3 h on 8 cores)
     python tests/golden/make_goldens.py --workload wan14b-i2v-block            # one 14B I2V block
     python tests/golden/make_goldens.py --workload wan1.3b-20step-sampler      # 20 steps on a shrunk latent
+    python tests/golden/make_goldens.py --workload wan1.3b-block --fp8 3       # the 8-bit variant of one block
 
-Outputs ``tests/golden/<workload>.npz`` (``-shrunk`` for the sampler; float32 values,
-int64 indices).
+Outputs ``tests/golden/<workload>.npz`` (``-shrunk`` for the sampler, ``-fp8`` for the
+8-bit variant; float32 values, int64 indices).
 """
 import argparse
 import os
@@ -36,8 +37,8 @@ def f32(a):
     return np.asarray(a, np.float32)
 
 
-def single_block(name, n_rows):
-    s = synth.WORKLOADS[name]
+def single_block(name, n_rows, fp8=0):
+    s = synth.WORKLOADS[name].replace(fp8=fp8)
     w = synth.make_weights(s, SEED)
     inp = synth.make_inputs(s, SEED)
     if s.text_dim:
@@ -89,13 +90,17 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", required=True, choices=["wan1.3b-block", "wan1.3b-30blk-guided-step",
                                                           "wan14b-i2v-block", "wan1.3b-20step-sampler"])
+    ap.add_argument("--fp8", type=int, default=0, help="8-bit variant bits (single-block workloads)")
     a = ap.parse_args()
     t0 = time.time()
     name = a.workload
-    if name == "wan1.3b-block":
-        out = single_block(name, 512)
-    elif name == "wan14b-i2v-block":
-        out = single_block(name, 256)
+    if a.fp8 and name not in ("wan1.3b-block", "wan14b-i2v-block"):
+        ap.error("--fp8 applies to the single-block workloads")
+    if name in ("wan1.3b-block", "wan14b-i2v-block"):
+        out = single_block(name, 512 if name == "wan1.3b-block" else 256, a.fp8)
+        if a.fp8:
+            name += "-fp8"
+            out["fp8"] = np.array(a.fp8, np.int64)
     elif name == "wan1.3b-30blk-guided-step":
         out = guided_step_full(512)
     else:

@@ -208,6 +208,10 @@ struct FwdWs {
   void *y, *qkv, *o, *qc, *kvc, *kvci, *h, *patchA;
   float *tsin, *h1, *e, *e0, *hm, *mods;
   float* rope;  // RoPE pair frequencies [head_dim / 2]
+  // 8-bit variant: LN output codes + row scales; attention operands (see Attn8Operands)
+  uint8_t *y8, *q8, *k8, *v8t;
+  float *sy, *sq, *sk, *sv;
+  unsigned int* vamax;
   size_t bytes;
 };
 
@@ -235,6 +239,23 @@ static FwdWs plan_forward(const wan_dit_config* cfg, void* ws) {
   w.hm = bp.take<float>(B * 2 * D);
   w.mods = bp.take<float>((long long)cfg->blocks * B * 6 * D);
   w.rope = bp.take<float>((size_t)hd / 2);
+  w.y8 = w.q8 = w.k8 = w.v8t = nullptr;
+  w.sy = w.sq = w.sk = w.sv = nullptr;
+  w.vamax = nullptr;
+  if (cfg->fp8 & 2) {
+    w.y8 = bp.take<uint8_t>(M * D);
+    w.sy = bp.take<float>(M);
+  }
+  if (cfg->fp8 & 1) {
+    const long long H = cfg->heads, nkb = (L + 127) / 128, Lp = round_up(L, 16);
+    w.q8 = bp.take<uint8_t>(M * D);
+    w.k8 = bp.take<uint8_t>(M * D);
+    w.v8t = bp.take<uint8_t>(B * H * hd * Lp);
+    w.sq = bp.take<float>(M * H);
+    w.sk = bp.take<float>(B * H * nkb);
+    w.sv = bp.take<float>(B * H * hd);
+    w.vamax = bp.take<unsigned int>(B * H * hd);
+  }
   w.bytes = (size_t)round_up((long long)bp.off, 1024);
   return w;
 }
@@ -260,6 +281,8 @@ static int validate_cfg(const wan_dit_config* cfg) {
   if (cfg->dtype == WAN_BF16 && cfg->head_dim != 64 && cfg->head_dim != 128) return WAN_ERR_UNSUPPORTED;
   if (cfg->dtype == WAN_F32 && (cfg->head_dim > 128 || cfg->head_dim % 2)) return WAN_ERR_UNSUPPORTED;
   if (cfg->freq_dim % 8) return WAN_ERR_UNSUPPORTED;
+  if (cfg->fp8 < 0 || cfg->fp8 > 3) return WAN_ERR_INVALID_ARG;
+  if (cfg->fp8 && (cfg->dtype != WAN_BF16 || cfg->head_dim != 128)) return WAN_ERR_UNSUPPORTED;
   return WAN_OK;
 }
 
@@ -278,6 +301,11 @@ static int validate_weights(const wan_dit_config* cfg, const wan_dit_weights* w)
     if (cfg->img_len && (!b.ckvi_w || !b.ckvi_b)) return WAN_ERR_INVALID_ARG;
     if (cfg->qk_norm && (!b.norm_q_w || !b.norm_k_w || !aligned16(b.norm_q_w) || !aligned16(b.norm_k_w)))
       return WAN_ERR_INVALID_ARG;
+    if (cfg->fp8 & 2) {
+      const void* f[] = {b.qkv_w8, b.qkv_ws, b.f1_w8, b.f1_ws};
+      for (const void* p : f)
+        if (!p || !aligned16(p)) return WAN_ERR_INVALID_ARG;
+    }
   }
   return WAN_OK;
 }
@@ -357,7 +385,11 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
     const float* mod = W.mods + (long long)i * B * 6 * D;  // [B][6][D]
 
     // --- self-attention: y = LN(x)(1+sc1)+sh1; q,k (RoPE), v; attention; x += g1 (o Wo^T + bo)
-    WAN_TRY(launch_ln_mod(c, W.x, mod + 0 * D, mod + 1 * D, 6LL * D, W.y, f32, M, L, D, cfg->eps));
+    const bool fp8_gemm = (cfg->fp8 & 2) != 0, fp8_attn = (cfg->fp8 & 1) != 0;
+    if (fp8_gemm)
+      WAN_TRY(launch_ln_mod_e4m3(c, W.x, mod + 0 * D, mod + 1 * D, 6LL * D, W.y8, W.sy, M, L, D, cfg->eps));
+    else
+      WAN_TRY(launch_ln_mod(c, W.x, mod + 0 * D, mod + 1 * D, 6LL * D, W.y, f32, M, L, D, cfg->eps));
     {
       EpiParams ep = epi_base(EPI_QKV, M, 3 * D, L, bw.qkv_b, f32);
       ep.out = W.qkv;
@@ -367,11 +399,33 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
       ep.n_f16 = f32 ? 0 : 2 * D;           // q, k feed the QK^T MMA in fp16
       ep.head_dim = hd;
       ep.rope = rg;
-      WAN_TRY(proj(c, f32, W.y, D, D, bw.qkv_w, D, D, M, 3 * D, D, 0, ep, "gemm_qkv_rope"));
+      if (fp8_gemm)
+        WAN_TRY(gemm_e4m3(c, W.y8, D, D, W.sy, static_cast<const uint8_t*>(bw.qkv_w8), D, D, bw.qkv_ws, M, 3 * D,
+                          D, ep, "gemm_qkv_rope_e4m3"));
+      else
+        WAN_TRY(proj(c, f32, W.y, D, D, bw.qkv_w, D, D, M, 3 * D, D, 0, ep, "gemm_qkv_rope"));
       if (cfg->qk_norm)
         WAN_TRY(launch_qk_rmsnorm_rope(c, W.qkv, 3LL * D, bw.norm_q_w, bw.norm_k_w, rg, M, L, D, hd, cfg->eps, f32));
     }
-    {
+    if (fp8_attn) {
+      Attn8Operands qa;
+      memset(&qa, 0, sizeof(qa));
+      qa.q = W.qkv; qa.ldq = 3LL * D; qa.q_col = 0;
+      qa.k = W.qkv; qa.ldk = 3LL * D; qa.k_col = D;
+      qa.v = W.qkv; qa.ldv = 3LL * D; qa.v_col = 2 * D;
+      qa.qk_type = OUT_F16; qa.v_type = OUT_BF16;
+      qa.B = B; qa.L = L; qa.H = H; qa.head_dim = hd;
+      qa.nkb = (L + 127) / 128; qa.Lp = (int)round_up(L, 16);
+      qa.q8 = W.q8; qa.sq = W.sq; qa.k8 = W.k8; qa.sk = W.sk; qa.v8t = W.v8t; qa.sv = W.sv; qa.v_amax = W.vamax;
+      WAN_TRY(quant_attn_e4m3(c, qa));
+      Attn8Args a;
+      memset(&a, 0, sizeof(a));
+      a.q8 = W.q8; a.sq = W.sq; a.k8 = W.k8; a.sk = W.sk; a.v8t = W.v8t; a.sv = W.sv;
+      a.o = W.o; a.ldo = D; a.o_col = 0;
+      a.B = B; a.L = L; a.H = H; a.head_dim = hd; a.Lp = qa.Lp;
+      a.tag = "attn_self_e4m3";
+      WAN_TRY(attention_e4m3(c, a));
+    } else {
       AttnArgs a;
       memset(&a, 0, sizeof(a));
       a.q = W.qkv; a.ldq = 3LL * D; a.q_row_len = 3 * D; a.q_col = 0;
@@ -433,13 +487,20 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
     }
 
     // --- FFN: y = LN(x)(1+sc2)+sh2; h = GELU(y W1^T + b1); x += g2 (h W2^T + b2)
-    WAN_TRY(launch_ln_mod(c, W.x, mod + 3 * D, mod + 4 * D, 6LL * D, W.y, f32, M, L, D, cfg->eps));
+    if (fp8_gemm)
+      WAN_TRY(launch_ln_mod_e4m3(c, W.x, mod + 3 * D, mod + 4 * D, 6LL * D, W.y8, W.sy, M, L, D, cfg->eps));
+    else
+      WAN_TRY(launch_ln_mod(c, W.x, mod + 3 * D, mod + 4 * D, 6LL * D, W.y, f32, M, L, D, cfg->eps));
     {
       EpiParams ep = epi_base(cfg->gelu_tanh ? EPI_GELU_TANH : EPI_GELU, M, Fh, L, bw.f1_b, f32);
       ep.out = W.h;
       ep.ldo = Fh;
       ep.out_type = f32 ? OUT_F32 : OUT_BF16;
-      WAN_TRY(proj(c, f32, W.y, D, D, bw.f1_w, D, D, M, Fh, D, 0, ep, "gemm_ffn1_gelu"));
+      if (fp8_gemm)
+        WAN_TRY(gemm_e4m3(c, W.y8, D, D, W.sy, static_cast<const uint8_t*>(bw.f1_w8), D, D, bw.f1_ws, M, Fh, D,
+                          ep, "gemm_ffn1_gelu_e4m3"));
+      else
+        WAN_TRY(proj(c, f32, W.y, D, D, bw.f1_w, D, D, M, Fh, D, 0, ep, "gemm_ffn1_gelu"));
     }
     {
       EpiParams ep = epi_base(EPI_RESID, M, D, L, bw.f2_b, f32);
@@ -685,6 +746,108 @@ int wan_linear(const void* x, const void* w, const void* b, void* out, int M, in
     ep.out_type = out_dtype == WAN_F32 ? OUT_F32 : (out_dtype == WAN_F16 ? OUT_F16 : OUT_BF16);
   }
   return proj(c, f32, x, K, K, w, K, K, M, N, K, 0, ep, "gemm_linear");
+}
+
+static int out_type_of(int dtype) {
+  return dtype == WAN_F32 ? OUT_F32 : (dtype == WAN_F16 ? OUT_F16 : OUT_BF16);
+}
+
+int wan_quant_rows_e4m3(const void* x, int dtype, long long ldx, int M, int K, void* x8, long long ld8, float* s,
+                        wan_stream_t stream) {
+  if (dtype != WAN_BF16 && dtype != WAN_F16 && dtype != WAN_F32) return WAN_ERR_INVALID_ARG;
+  if (!x || !x8 || !s || M < 0 || K <= 0 || ldx < K || ld8 < K) return WAN_ERR_INVALID_ARG;
+  if (K % 4 || ldx % 4 || ld8 % 4 || !aligned16(x) || (reinterpret_cast<uintptr_t>(x8) & 3)) return WAN_ERR_UNSUPPORTED;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  return launch_quant_rows_e4m3(c, x, out_type_of(dtype), ldx, M, K, static_cast<uint8_t*>(x8), ld8, s);
+}
+
+size_t wan_quant_attn_workspace_size(int B, int H, int d) {
+  if (B <= 0 || H <= 0 || d <= 0) return 0;
+  return (size_t)round_up((long long)B * H * d * 4, 1024);
+}
+
+int wan_quant_attn_e4m3(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int B, int L, int H,
+                        int d, void* q8, float* sq, void* k8, float* sk, void* v8t, float* sv, void* ws,
+                        size_t ws_bytes, wan_stream_t stream) {
+  if ((qk_dtype != WAN_BF16 && qk_dtype != WAN_F16) || (v_dtype != WAN_BF16 && v_dtype != WAN_F16))
+    return WAN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !q8 || !sq || !k8 || !sk || !v8t || !sv || B <= 0 || L <= 0 || H <= 0)
+    return WAN_ERR_INVALID_ARG;
+  if (d != 128) return WAN_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q, k, v, q8, k8, v8t};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return WAN_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < wan_quant_attn_workspace_size(B, H, d)) return WAN_ERR_WORKSPACE;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  Attn8Operands a;
+  memset(&a, 0, sizeof(a));
+  const int D = H * d;
+  a.q = q; a.ldq = D; a.q_col = 0;
+  a.k = k; a.ldk = D; a.k_col = 0;
+  a.v = v; a.ldv = D; a.v_col = 0;
+  a.qk_type = out_type_of(qk_dtype);
+  a.v_type = out_type_of(v_dtype);
+  a.B = B; a.L = L; a.H = H; a.head_dim = d;
+  a.nkb = (L + 127) / 128;
+  a.Lp = (int)round_up(L, 16);
+  a.q8 = static_cast<uint8_t*>(q8); a.sq = sq;
+  a.k8 = static_cast<uint8_t*>(k8); a.sk = sk;
+  a.v8t = static_cast<uint8_t*>(v8t); a.sv = sv;
+  a.v_amax = static_cast<unsigned int*>(ws);
+  return quant_attn_e4m3(c, a);
+}
+
+int wan_attn_e4m3(const void* q8, const float* sq, const void* k8, const float* sk, const void* v8t, const float* sv,
+                  void* o, const int* kv_lens, int B, int L, int H, int d, wan_stream_t stream) {
+  if (!q8 || !sq || !k8 || !sk || !v8t || !sv || !o || B <= 0 || L <= 0 || H <= 0) return WAN_ERR_INVALID_ARG;
+  if (d != 128) return WAN_ERR_UNSUPPORTED;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8t) || !aligned16(sv) || !aligned16(o))
+    return WAN_ERR_UNSUPPORTED;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  Attn8Args a;
+  memset(&a, 0, sizeof(a));
+  a.q8 = static_cast<const uint8_t*>(q8); a.sq = sq;
+  a.k8 = static_cast<const uint8_t*>(k8); a.sk = sk;
+  a.v8t = static_cast<const uint8_t*>(v8t); a.sv = sv;
+  a.o = o; a.ldo = (long long)H * d; a.o_col = 0;
+  a.B = B; a.L = L; a.H = H; a.head_dim = d; a.Lp = (int)round_up(L, 16);
+  a.kv_lens = kv_lens;
+  a.tag = "attn_self_e4m3";
+  return attention_e4m3(c, a);
+}
+
+int wan_linear_e4m3(const void* x8, const float* sx, const void* w8, const float* sw, const void* b, void* out, int M,
+                    int N, int K, int epilogue, const float* gate, int rows_per_gate, wan_stream_t stream) {
+  if (!x8 || !sx || !w8 || !sw || !out || M <= 0 || N <= 0 || K <= 0) return WAN_ERR_INVALID_ARG;
+  if (epilogue != WAN_EPI_STORE && epilogue != WAN_EPI_GELU && epilogue != WAN_EPI_RESIDUAL &&
+      epilogue != WAN_EPI_GELU_TANH)
+    return WAN_ERR_INVALID_ARG;
+  if (gate && rows_per_gate <= 0) return WAN_ERR_INVALID_ARG;
+  if (N % 32 || K % 16 || !aligned16(x8) || !aligned16(w8) || !aligned16(sw) || !aligned16(out) ||
+      (gate && !aligned16(gate)) || (b && !aligned16(b)))
+    return WAN_ERR_UNSUPPORTED;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  const int kind = epilogue == WAN_EPI_STORE ? EPI_STORE
+                   : epilogue == WAN_EPI_GELU ? EPI_GELU
+                   : epilogue == WAN_EPI_GELU_TANH ? EPI_GELU_TANH
+                                                   : EPI_RESID;
+  EpiParams ep = epi_base(kind, M, N, gate ? rows_per_gate : M, b, 0);
+  if (kind == EPI_RESID) {
+    ep.resid = static_cast<float*>(out);
+    ep.ldr = N;
+    ep.gate = gate;
+    ep.ld_gate = N;
+  } else {
+    ep.out = out;
+    ep.ldo = N;
+    ep.out_type = OUT_BF16;
+  }
+  return gemm_e4m3(c, static_cast<const uint8_t*>(x8), K, K, sx, static_cast<const uint8_t*>(w8), K, K, sw, M, N, K,
+                   ep, "gemm_linear_e4m3");
 }
 
 size_t wan_text_embed_workspace_size(int B, int Lt, int D, int dtype) {

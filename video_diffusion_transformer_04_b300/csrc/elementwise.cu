@@ -13,7 +13,8 @@ namespace wan {
 template <int NV, typename OutT>
 __global__ void __launch_bounds__(128) ln_mod_kernel(const float* __restrict__ x, const float* __restrict__ shift,
                                                      const float* __restrict__ scale, long long mod_bstride,
-                                                     OutT* __restrict__ y, int L, int D, float eps) {
+                                                     OutT* __restrict__ y, float* __restrict__ sy, int L, int D,
+                                                     float eps) {
   __shared__ float red[4];
   const int row = blockIdx.x;
   const int b = row / L;
@@ -49,38 +50,65 @@ __global__ void __launch_bounds__(128) ln_mod_kernel(const float* __restrict__ x
   const float rstd = rsqrtf(var + eps);
   const float* sh = shift ? shift + (long long)b * mod_bstride : nullptr;
   const float* sc = scale ? scale + (long long)b * mod_bstride : nullptr;
+  float o[NV][4];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = t + i * 128;
+    o[i][0] = (v[i].x - mean) * rstd; o[i][1] = (v[i].y - mean) * rstd;
+    o[i][2] = (v[i].z - mean) * rstd; o[i][3] = (v[i].w - mean) * rstd;
+    if (c >= nv4) continue;
+    if (sc) {
+      const float4 s4 = reinterpret_cast<const float4*>(sc)[c];
+      o[i][0] *= 1.f + s4.x; o[i][1] *= 1.f + s4.y; o[i][2] *= 1.f + s4.z; o[i][3] *= 1.f + s4.w;
+    }
+    if (sh) {
+      const float4 h4 = reinterpret_cast<const float4*>(sh)[c];
+      o[i][0] += h4.x; o[i][1] += h4.y; o[i][2] += h4.z; o[i][3] += h4.w;
+    }
+  }
+  // E4M3 output: per-row scale from the row's |max| (decided in fp32).
+  float inv = 0.f;
+  if constexpr (sizeof(OutT) == 1) {
+    float a = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (t + i * 128 < nv4)
+        a = fmaxf(a, fmaxf(fmaxf(fabsf(o[i][0]), fabsf(o[i][1])), fmaxf(fabsf(o[i][2]), fabsf(o[i][3]))));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    __syncthreads();
+    if ((t & 31) == 0) red[t >> 5] = a;
+    __syncthreads();
+    a = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    inv = e4m3_inv(a);
+    if (t == 0) sy[row] = e4m3_deq(a);
+  }
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int c = t + i * 128;
     if (c >= nv4) continue;
-    float o[4] = {(v[i].x - mean) * rstd, (v[i].y - mean) * rstd, (v[i].z - mean) * rstd, (v[i].w - mean) * rstd};
-    if (sc) {
-      const float4 s4 = reinterpret_cast<const float4*>(sc)[c];
-      o[0] *= 1.f + s4.x; o[1] *= 1.f + s4.y; o[2] *= 1.f + s4.z; o[3] *= 1.f + s4.w;
-    }
-    if (sh) {
-      const float4 h4 = reinterpret_cast<const float4*>(sh)[c];
-      o[0] += h4.x; o[1] += h4.y; o[2] += h4.z; o[3] += h4.w;
-    }
     if constexpr (sizeof(OutT) == 4) {
-      reinterpret_cast<float4*>(y + (long long)row * D)[c] = make_float4(o[0], o[1], o[2], o[3]);
-    } else {
+      reinterpret_cast<float4*>(y + (long long)row * D)[c] = make_float4(o[i][0], o[i][1], o[i][2], o[i][3]);
+    } else if constexpr (sizeof(OutT) == 2) {
       uint2 u;
-      u.x = pack_bf16x2(o[0], o[1]);
-      u.y = pack_bf16x2(o[2], o[3]);
+      u.x = pack_bf16x2(o[i][0], o[i][1]);
+      u.y = pack_bf16x2(o[i][2], o[i][3]);
       reinterpret_cast<uint2*>(y + (long long)row * D)[c] = u;
+    } else {
+      reinterpret_cast<uint32_t*>(y + (long long)row * D)[c] =
+          e4m3x4(__fmul_rn(o[i][0], inv), __fmul_rn(o[i][1], inv), __fmul_rn(o[i][2], inv), __fmul_rn(o[i][3], inv));
     }
   }
 }
 
 template <typename OutT>
 static void ln_dispatch(const LaunchCtx& c, const float* x, const float* sh, const float* sc, long long bs, OutT* y,
-                        int rows, int L, int D, float eps) {
+                        float* sy, int rows, int L, int D, float eps) {
   const int nv = (D / 4 + 127) / 128;
-  if (nv <= 1) ln_mod_kernel<1, OutT><<<rows, 128, 0, c.stream>>>(x, sh, sc, bs, y, L, D, eps);
-  else if (nv <= 3) ln_mod_kernel<3, OutT><<<rows, 128, 0, c.stream>>>(x, sh, sc, bs, y, L, D, eps);
-  else if (nv <= 10) ln_mod_kernel<10, OutT><<<rows, 128, 0, c.stream>>>(x, sh, sc, bs, y, L, D, eps);
-  else ln_mod_kernel<16, OutT><<<rows, 128, 0, c.stream>>>(x, sh, sc, bs, y, L, D, eps);
+  if (nv <= 1) ln_mod_kernel<1, OutT><<<rows, 128, 0, c.stream>>>(x, sh, sc, bs, y, sy, L, D, eps);
+  else if (nv <= 3) ln_mod_kernel<3, OutT><<<rows, 128, 0, c.stream>>>(x, sh, sc, bs, y, sy, L, D, eps);
+  else if (nv <= 10) ln_mod_kernel<10, OutT><<<rows, 128, 0, c.stream>>>(x, sh, sc, bs, y, sy, L, D, eps);
+  else ln_mod_kernel<16, OutT><<<rows, 128, 0, c.stream>>>(x, sh, sc, bs, y, sy, L, D, eps);
 }
 
 int launch_ln_mod(const LaunchCtx& c, const float* x, const float* shift, const float* scale, long long mod_bstride,
@@ -88,9 +116,19 @@ int launch_ln_mod(const LaunchCtx& c, const float* x, const float* shift, const 
   if (rows <= 0) return WAN_OK;
   if (D % 4 != 0 || D > 8192) return WAN_ERR_UNSUPPORTED;
   count_launch("ln_modulate", c.stream, true);
-  if (out_f32) ln_dispatch<float>(c, x, shift, scale, mod_bstride, static_cast<float*>(y), rows, L, D, eps);
-  else ln_dispatch<bf16>(c, x, shift, scale, mod_bstride, static_cast<bf16*>(y), rows, L, D, eps);
+  if (out_f32) ln_dispatch<float>(c, x, shift, scale, mod_bstride, static_cast<float*>(y), nullptr, rows, L, D, eps);
+  else ln_dispatch<bf16>(c, x, shift, scale, mod_bstride, static_cast<bf16*>(y), nullptr, rows, L, D, eps);
   count_launch("ln_modulate", c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+int launch_ln_mod_e4m3(const LaunchCtx& c, const float* x, const float* shift, const float* scale,
+                       long long mod_bstride, uint8_t* y8, float* sy, int rows, int L, int D, float eps) {
+  if (rows <= 0) return WAN_OK;
+  if (D % 4 != 0 || D > 8192) return WAN_ERR_UNSUPPORTED;
+  count_launch("ln_modulate_e4m3", c.stream, true);
+  ln_dispatch<uint8_t>(c, x, shift, scale, mod_bstride, y8, sy, rows, L, D, eps);
+  count_launch("ln_modulate_e4m3", c.stream, false);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
 

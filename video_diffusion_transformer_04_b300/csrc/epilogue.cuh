@@ -50,6 +50,9 @@ struct EpiParams {
   // EPI_HEAD
   float* vout;
   int C, F, H, W;
+  // FP8 GEMM: acc[m, n] * a_scale[m] * b_scale[n] before everything above
+  const float* a_scale;
+  const float* b_scale;
 };
 
 // v[i] += bias[n0 + i] with 16-byte vector loads (bias rows are 16-byte aligned and n0

@@ -1,6 +1,9 @@
 // bf16 GEMM on the 5th-generation tensor cores: C[M, N] = A[M, K] * B[N, K]^T with a
 // fused epilogue (epilogue.cuh).  Every projection of the DiT block (QKV, output,
 // cross-attention, FFN, patchify, head, text projection) runs through this kernel.
+// The FP8 instantiation (E4M3 A and B, kind::f8f6f4, 128 elements per 128-byte stage row)
+// multiplies the fp32 accumulator by the row scale of A and the column scale of B before
+// the same epilogue.
 //
 // Design (one CTA per SM, persistent over output tiles of 128 x BN):
 //   warp 0      TMA producer: A and B tiles (128-byte swizzle) into a STAGES-deep ring
@@ -27,9 +30,9 @@ namespace wan {
 template <int BN>
 struct GemmCfg {
   static constexpr int BM = 128;
-  static constexpr int BK = 64;  // one 128-byte swizzle row of bf16
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int BK_BYTES = 128;  // one 128-byte swizzle row: 64 bf16 or 128 E4M3
+  static constexpr int A_BYTES = BM * BK_BYTES;
+  static constexpr int B_BYTES = BN * BK_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
   static constexpr int TMEM_COLS = 2 * BN;
@@ -42,12 +45,13 @@ struct GemmCfg {
   static_assert(SMEM <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
-template <int BN>
+template <int BN, bool FP8>
 __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmR, const EpiParams ep, int M, int N, int K,
                         int kb_period, int* status) {
   using Cfg = GemmCfg<BN>;
+  constexpr int BK = FP8 ? 128 : 64;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi_stage = smem + Cfg::STAGES * Cfg::STAGE_BYTES;
@@ -62,7 +66,7 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
   const int lane = threadIdx.x & 31;
   const int num_m = (M + Cfg::BM - 1) / Cfg::BM;
   const int num_n = (N + BN - 1) / BN;
-  const int num_k = (K + Cfg::BK - 1) / Cfg::BK;
+  const int num_k = (K + BK - 1) / BK;
   const int num_tiles = num_m * num_n;
 
   if (threadIdx.x == 0) {
@@ -101,8 +105,8 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
         uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
         mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
         const int kb_b = kb_period ? (kb % kb_period) : kb;
-        tma_load_2d(sa, &tmA, &full[stage], kb * Cfg::BK, mb * Cfg::BM);
-        tma_load_2d(sa + Cfg::A_BYTES, &tmB, &full[stage], kb_b * Cfg::BK, nb * BN);
+        tma_load_2d(sa, &tmA, &full[stage], kb * BK, mb * Cfg::BM);
+        tma_load_2d(sa + Cfg::A_BYTES, &tmB, &full[stage], kb_b * BK, nb * BN);
         issued |= 1u << stage;
         issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1; }
@@ -117,7 +121,7 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc = make_idesc_bf16(Cfg::BM, BN);
+    constexpr uint32_t idesc = FP8 ? make_idesc_e4m3(Cfg::BM, BN) : make_idesc_bf16(Cfg::BM, BN);
     const uint32_t smem_lo0 = sdesc_sw128_lo(smem_u32(smem));
     int stage = 0;
     uint32_t phase = 0;
@@ -132,12 +136,17 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
         if (!mbar_wait(&full[stage], phase, status, kDevTimeoutGemm)) { ok = false; break; }
         tc_fence_after();
         // Descriptor low words only (the issuing thread shares its SM sub-partition with
-        // an epilogue warp): stage base + 32 bytes (>> 4 = 2) per K step of 16.
+        // an epilogue warp): stage base + 32 bytes (>> 4 = 2) per MMA K step (16 bf16 or
+        // 32 E4M3 elements).
         const uint32_t a_lo = smem_lo0 + (uint32_t)stage * (Cfg::STAGE_BYTES >> 4);
         const uint32_t b_lo = a_lo + (Cfg::A_BYTES >> 4);
 #pragma unroll
-        for (int kk = 0; kk < Cfg::BK / 16; ++kk)
-          tc_mma_ss_lo(d_tmem, a_lo + kk * 2, b_lo + kk * 2, idesc, (kb | kk) != 0 ? 1u : 0u);
+        for (int kk = 0; kk < Cfg::BK_BYTES / 32; ++kk) {
+          if constexpr (FP8)
+            tc_mma_ss_f8_lo(d_tmem, a_lo + kk * 2, b_lo + kk * 2, idesc, (kb | kk) != 0 ? 1u : 0u);
+          else
+            tc_mma_ss_lo(d_tmem, a_lo + kk * 2, b_lo + kk * 2, idesc, (kb | kk) != 0 ? 1u : 0u);
+        }
         tc_commit(&empty[stage]);
         if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1; }
       }
@@ -167,6 +176,24 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
       const int row0 = mb * Cfg::BM + quad * 32;
       const int row = row0 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
+      float sa_row = 1.f;
+      if constexpr (FP8) sa_row = row < M ? ep.a_scale[row] : 0.f;
+      // fp32 accumulator chunk -> v (times the A row and B column scales of the FP8 GEMM)
+      auto acc_values = [&](const uint32_t (&r)[32], int n0, float (&v)[32]) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        if constexpr (FP8) {
+          const float4* sb4 = reinterpret_cast<const float4*>(ep.b_scale + n0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 q = sb4[i];
+            v[4 * i] *= sa_row * q.x;
+            v[4 * i + 1] *= sa_row * q.y;
+            v[4 * i + 2] *= sa_row * q.z;
+            v[4 * i + 3] *= sa_row * q.w;
+          }
+        }
+      };
 #pragma unroll 1
       for (int c = ehalf * CH; c < (ehalf + 1) * CH; ++c) {
         uint32_t r[32];
@@ -175,8 +202,7 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
         if (tma_resid) {
           if (row0 < M && n0 < N) {  // warp-uniform; rows past M are clipped by the TMA
             float v[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            acc_values(r, n0, v);
             epi_resid_values<32>(ep, row, n0, v);
             float* buf = stage;
             if (lane == 0) bulk_wait_group_read<0>();  // the reduce that last read `buf` is done
@@ -194,8 +220,7 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
           }
         } else if (row < M && n0 < N) {
           float v[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          acc_values(r, n0, v);
           epilogue_chunk<32>(ep, row, n0, v);
         }
       }
@@ -215,13 +240,13 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
   if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
-template <int BN>
+template <int BN, bool FP8>
 static int launch_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr,
                        const EpiParams& ep, int M, int N, int K, int kb_period, const char* tag) {
   using Cfg = GemmCfg<BN>;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
+    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<BN, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
         cudaSuccess)
       return WAN_ERR_CUDA;
     attr_set = true;
@@ -229,8 +254,8 @@ static int launch_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensor
   const int tiles = ((M + 127) / 128) * ((N + BN - 1) / BN);
   const int grid = tiles < c.num_sms ? tiles : c.num_sms;
   count_launch(tag, c.stream, true);
-  gemm_bf16_tc_kernel<BN><<<grid, Cfg::THREADS, Cfg::SMEM, c.stream>>>(ta, tb, tr, ep, M, N, K, kb_period,
-                                                                       c.dev_status);
+  gemm_bf16_tc_kernel<BN, FP8><<<grid, Cfg::THREADS, Cfg::SMEM, c.stream>>>(ta, tb, tr, ep, M, N, K, kb_period,
+                                                                            c.dev_status);
   count_launch(tag, c.stream, false);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
@@ -255,9 +280,39 @@ int gemm_bf16(const LaunchCtx& c, const bf16* A, long long lda, int a_cols, cons
     if (st != WAN_OK) return st;
   }
   switch (bn) {
-    case 256: return launch_gemm<256>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
-    case 128: return launch_gemm<128>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
-    default: return launch_gemm<64>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
+    case 256: return launch_gemm<256, false>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
+    case 128: return launch_gemm<128, false>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
+    default: return launch_gemm<64, false>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
+  }
+}
+
+int gemm_e4m3(const LaunchCtx& c, const uint8_t* A, long long lda, int a_cols, const float* sa, const uint8_t* B,
+              long long ldb, int b_cols, const float* sb, int M, int N, int K, const EpiParams& ep_in, const char* tag) {
+  if (M <= 0 || N <= 0 || K <= 0) return WAN_OK;
+  if (!sa || !sb || (reinterpret_cast<uintptr_t>(sb) & 15) || N % 32) return WAN_ERR_UNSUPPORTED;
+  const int bn = (N % 256 == 0) ? 256 : (N % 128 == 0 ? 128 : 64);
+  CUtensorMap ta, tb;
+  int st = make_tmap_2d(&ta, A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)a_cols, (uint64_t)M, (uint64_t)lda, 128,
+                        128);
+  if (st != WAN_OK) return st;
+  st = make_tmap_2d(&tb, B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)b_cols, (uint64_t)N, (uint64_t)ldb, 128,
+                    (uint32_t)bn);
+  if (st != WAN_OK) return st;
+  EpiParams ep = ep_in;
+  ep.a_scale = sa;
+  ep.b_scale = sb;
+  CUtensorMap tr;
+  memset(&tr, 0, sizeof(tr));
+  if (ep.kind == EPI_RESID) {
+    if (ep.ldr % 4 != 0) return WAN_ERR_UNSUPPORTED;
+    st = make_tmap_2d(&tr, ep.resid, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)N, (uint64_t)M,
+                      (uint64_t)ep.ldr * 4, 32, 32);
+    if (st != WAN_OK) return st;
+  }
+  switch (bn) {
+    case 256: return launch_gemm<256, true>(c, ta, tb, tr, ep, M, N, K, 0, tag);
+    case 128: return launch_gemm<128, true>(c, ta, tb, tr, ep, M, N, K, 0, tag);
+    default: return launch_gemm<64, true>(c, ta, tb, tr, ep, M, N, K, 0, tag);
   }
 }
 

@@ -20,6 +20,11 @@ int make_tmap_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int e
 // kb_period > 0: the B k-block index wraps modulo kb_period (A = [hi | lo] split).
 int gemm_bf16(const LaunchCtx& c, const bf16* A, long long lda, int a_cols, const bf16* B, long long ldb,
               int b_cols, int M, int N, int K, int kb_period, const EpiParams& ep, const char* tag);
+// FP8 (E4M3) tcgen05 GEMM: C = (A8 sa) (B8 sb)^T -> epilogue, with per-row scales sa [M]
+// of A and per-row scales sb [N] of B (per output channel) applied to the fp32
+// accumulator before the epilogue.  lda / ldb: row strides in bytes (multiples of 16).
+int gemm_e4m3(const LaunchCtx& c, const uint8_t* A, long long lda, int a_cols, const float* sa, const uint8_t* B,
+              long long ldb, int b_cols, const float* sb, int M, int N, int K, const EpiParams& ep, const char* tag);
 // fp32 SIMT GEMM (parity path): same contract, fp32 operands.
 int gemm_f32(const LaunchCtx& c, const float* A, long long lda, const float* B, long long ldb, int M, int N, int K,
              const EpiParams& ep, const char* tag);
@@ -49,6 +54,53 @@ struct AttnArgs {
 };
 int attention_bf16(const LaunchCtx& c, const AttnArgs& a);
 int attention_f32(const LaunchCtx& c, const AttnArgs& a);
+
+// ------------------------------------------------------------------ 8-bit operands and attention
+// Quantiser inputs (q, k, v rows of the QKV projection, bf16 or fp16) and outputs.
+struct Attn8Operands {
+  const void* q;
+  long long ldq;  // row stride (elements)
+  int q_col;      // column of head 0
+  const void* k;
+  long long ldk;
+  int k_col;
+  const void* v;
+  long long ldv;
+  int v_col;
+  int qk_type, v_type;  // OutType of the inputs: OUT_BF16 or OUT_F16
+  int B, L, H, head_dim;
+  int nkb;  // ceil(L / 128)
+  int Lp;   // L rounded up to 16
+  uint8_t* q8;  // [B*L, H*d]
+  float* sq;    // [B*L, H]
+  uint8_t* k8;  // [B*L, H*d]
+  float* sk;    // [B, H, nkb]
+  uint8_t* v8t; // [B, H, d, Lp]
+  float* sv;    // [B, H, d]
+  unsigned int* v_amax;  // [B, H, d] scratch
+};
+int quant_attn_e4m3(const LaunchCtx& c, const Attn8Operands& a);
+struct Attn8Args {
+  const uint8_t* q8;
+  const float* sq;
+  const uint8_t* k8;
+  const float* sk;
+  const uint8_t* v8t;
+  const float* sv;
+  void* o;  // bf16 [B, L, ldo], head h at columns o_col + h*d
+  long long ldo;
+  int o_col;
+  int B, L, H, head_dim, Lp;
+  const int* kv_lens;  // device [B] or NULL
+  const char* tag;
+};
+int attention_e4m3(const LaunchCtx& c, const Attn8Args& a);
+// x8[r, :] = E4M3 codes of row r of x (in_type OutType), s[r] its dequantisation scale.
+int launch_quant_rows_e4m3(const LaunchCtx& c, const void* x, int in_type, long long ldx, int rows, int K,
+                           uint8_t* x8, long long ld8, float* s);
+// LN + modulation (as launch_ln_mod) written as per-row E4M3 codes y8 [rows, D] and scales sy [rows].
+int launch_ln_mod_e4m3(const LaunchCtx& c, const float* x, const float* shift, const float* scale,
+                       long long mod_bstride, uint8_t* y8, float* sy, int rows, int L, int D, float eps);
 
 // ------------------------------------------------------------------ elementwise / small kernels
 int launch_ln_mod(const LaunchCtx& c, const float* x, const float* shift, const float* scale, long long mod_bstride,

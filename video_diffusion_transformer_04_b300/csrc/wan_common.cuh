@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -19,6 +20,7 @@ enum DevStatus : int {
   kDevOk = 0,
   kDevTimeoutGemm = 0x101,
   kDevTimeoutAttn = 0x102,
+  kDevTimeoutAttn8 = 0x103,
   kDevTimeoutSelftest = 0x1ff,
 };
 
@@ -266,6 +268,30 @@ __device__ __forceinline__ void tc_mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// The same two forms with kind::f8f6f4: 8-bit A and B (the instruction descriptor's A/B
+// format fields 0 = E4M3), fp32 accumulate, K = 32 per instruction (32 bytes of a
+// 128-byte swizzle row, like K = 16 of a 16-bit type).
+__device__ __forceinline__ void tc_mma_ss_f8_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .b64 da, db;\n .reg .pred p;\n mov.b64 da, {%1, %5};\n mov.b64 db, {%2, %5};\n"
+      " setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kSdescSw128Hi)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_ts_f8_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .b64 db;\n .reg .pred p;\n mov.b64 db, {%2, %5};\n"
+      " setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kSdescSw128Hi)
+      : "memory");
+}
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format 0), both K-major, fp32 D.
+__host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 #define WAN_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), \
                   "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
 #define WAN_S8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), \
@@ -317,7 +343,26 @@ __device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t*
       WAN_S8(0), WAN_S8(8)
       : "memory");
 }
+__device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      WAN_S8(0), WAN_S8(8), WAN_S8(16), WAN_S8(24)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
+// ------------------------------------------------------------------ E4M3 (OCP FP8)
+// Two floats -> two E4M3 bytes, the first in the low byte (round to nearest even,
+// saturating at +-448).
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  return e4m3x2(a, b) | (e4m3x2(c, d) << 16);
+}
+__device__ __forceinline__ float e4m3_inv(float amax) { return amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f; }
+__device__ __forceinline__ float e4m3_deq(float amax) { return __fdiv_rn(amax, 448.f); }
 
 // Register budget of a warpgroup after launch (all 128 threads execute it).
 template <int N>

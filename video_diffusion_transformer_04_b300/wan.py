@@ -42,11 +42,13 @@ P, I, LL, F, SZ = C.c_void_p, C.c_int, C.c_longlong, C.c_float, C.c_size_t
 class wan_dit_config(C.Structure):
     _fields_ = [("dtype", I), ("batch", I), ("c_in", I), ("c_out", I), ("frames", I), ("height", I), ("width", I),
                 ("dim", I), ("heads", I), ("head_dim", I), ("ffn", I), ("blocks", I), ("text_len", I),
-                ("img_len", I), ("freq_dim", I), ("theta", F), ("eps", F), ("qk_norm", I), ("gelu_tanh", I)]
+                ("img_len", I), ("freq_dim", I), ("theta", F), ("eps", F), ("qk_norm", I), ("gelu_tanh", I),
+                ("fp8", I)]
 
 
 _BLOCK_FIELDS = ["mod", "qkv_w", "qkv_b", "o_w", "o_b", "cq_w", "cq_b", "ckv_w", "ckv_b", "ckvi_w", "ckvi_b",
-                 "co_w", "co_b", "f1_w", "f1_b", "f2_w", "f2_b", "norm_q_w", "norm_k_w"]
+                 "co_w", "co_b", "f1_w", "f1_b", "f2_w", "f2_b", "norm_q_w", "norm_k_w",
+                 "qkv_w8", "qkv_ws", "f1_w8", "f1_ws"]
 _GLOBAL_FIELDS = ["patch_w", "patch_b", "t1_w", "t1_b", "t2_w", "t2_b", "m_w", "m_b", "hm_w", "hm_b", "head_w",
                   "head_b"]
 
@@ -87,6 +89,11 @@ _SIGS = {
     "wan_dit_guided_step": (I, [C.POINTER(wan_dit_config), C.POINTER(wan_dit_weights), P, P, F, P, P, P, P, P,
                                 SZ, P]),
     "wan_sample": (I, [C.POINTER(wan_dit_config), C.POINTER(wan_dit_weights), P, I, F, P, P, P, P, P, P, SZ, P]),
+    "wan_quant_rows_e4m3": (I, [P, I, LL, I, I, P, LL, P, P]),
+    "wan_quant_attn_workspace_size": (SZ, [I, I, I]),
+    "wan_quant_attn_e4m3": (I, [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, SZ, P]),
+    "wan_attn_e4m3": (I, [P, P, P, P, P, P, P, P, I, I, I, I, P]),
+    "wan_linear_e4m3": (I, [P, P, P, P, P, P, I, I, I, I, P, I, P]),
     "wan_profile_begin": (I, [I]),
     "wan_profile_end": (I, [C.POINTER(C.c_char_p), C.POINTER(C.c_double), C.POINTER(C.c_int), I]),
 }
@@ -205,6 +212,38 @@ def wan_linear(x, w, b, out, epilogue=WAN_EPI_STORE, gate=None, rows_per_gate=0,
                           dtype_code(x.dtype), dtype_code(out.dtype), _stream(stream)), "wan_linear")
 
 
+def wan_quant_rows_e4m3(x, x8, s, stream=None):
+    """x [M, K] (bf16 / fp16 / fp32) -> E4M3 codes x8 [M, K] (uint8) and row scales s [M]."""
+    M, K = x.shape
+    _check(lib.wan_quant_rows_e4m3(_p(x), dtype_code(x.dtype), x.stride(0), M, K, _p(x8), x8.stride(0), _p(s),
+                                   _stream(stream)), "wan_quant_rows_e4m3")
+
+
+def wan_quant_attn_workspace_size(B, H, d):
+    return lib.wan_quant_attn_workspace_size(B, H, d)
+
+
+def wan_quant_attn_e4m3(q, k, v, q8, sq, k8, sk, v8t, sv, ws, stream=None):
+    """q, k, v [B, L, H, d] -> q8 [B, L, H, d], sq [B, L, H], k8, sk [B, H, nkb], v8t [B, H, d, Lp], sv [B, H, d]."""
+    B, L, H, d = q.shape
+    _check(lib.wan_quant_attn_e4m3(_p(q), _p(k), _p(v), dtype_code(q.dtype), dtype_code(v.dtype), B, L, H, d, _p(q8),
+                                   _p(sq), _p(k8), _p(sk), _p(v8t), _p(sv), _p(ws), _nbytes(ws), _stream(stream)),
+           "wan_quant_attn_e4m3")
+
+
+def wan_attn_e4m3(q8, sq, k8, sk, v8t, sv, o, kv_lens=None, stream=None):
+    B, L, H, d = q8.shape
+    _check(lib.wan_attn_e4m3(_p(q8), _p(sq), _p(k8), _p(sk), _p(v8t), _p(sv), _p(o), _p(kv_lens), B, L, H, d,
+                             _stream(stream)), "wan_attn_e4m3")
+
+
+def wan_linear_e4m3(x8, sx, w8, sw, b, out, epilogue=WAN_EPI_STORE, gate=None, rows_per_gate=0, stream=None):
+    M, K = x8.shape
+    N = w8.shape[0]
+    _check(lib.wan_linear_e4m3(_p(x8), _p(sx), _p(w8), _p(sw), _p(b), _p(out), M, N, K, epilogue, _p(gate),
+                               rows_per_gate, _stream(stream)), "wan_linear_e4m3")
+
+
 def wan_text_embed_workspace_size(B, Lt, D, dtype):
     return lib.wan_text_embed_workspace_size(B, Lt, D, dtype)
 
@@ -300,10 +339,17 @@ class DiT:
             heads=shape.heads, head_dim=shape.head_dim, ffn=shape.ffn, blocks=shape.blocks,
             text_len=shape.text_len, img_len=shape.img_len, freq_dim=shape.freq_dim, theta=shape.theta,
             eps=shape.eps, qk_norm=int(getattr(shape, "qk_norm", False)),
-            gelu_tanh=int(getattr(shape, "gelu_tanh", False)))
+            gelu_tanh=int(getattr(shape, "gelu_tanh", False)), fp8=int(getattr(shape, "fp8", 0)))
         up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=self.tdtype)
         self.tensors = {k: up(v) for k, v in weights.items() if k != "blocks"}
         self.block_tensors = [{k: up(v) for k, v in blk.items()} for blk in weights["blocks"]]
+        if self.cfg.fp8 & 2:  # E4M3 codes + per-output-channel scales of the QKV and FFN-up weights
+            for bt in self.block_tensors:
+                for n in ("qkv_w", "f1_w"):
+                    w = bt[n]
+                    bt[n + "8"] = torch.empty(w.shape, dtype=torch.uint8, device=device)
+                    bt[n[:-1] + "ws"] = torch.empty(w.shape[0], dtype=torch.float32, device=device)
+                    wan_quant_rows_e4m3(w, bt[n + "8"], bt[n[:-1] + "ws"])
         self.blocks_c = (wan_block_weights * len(self.block_tensors))()
         for i, bt in enumerate(self.block_tensors):
             for n in _BLOCK_FIELDS:
