@@ -12,11 +12,13 @@
   with p_j the exact probabilities relative to the row max.
 * FP8 GEMM, fed the oracle's codes: every product of two codes is exact, the sum is fp32,
   so the bf16 tolerances of the other GEMMs apply (fp32 tolerance for the residual form).
-* The forward with the variant on, against the oracle's 8-bit forward: the GPU's
-  activations are bf16 where the oracle's are fp64, so a few codes straddle a rounding
-  boundary differently, and the kernel's probability rounding is not modelled; the test
-  requires the GPU to be no farther from the oracle's 8-bit result than that result is
-  from the exact (unquantised) model.
+* The forward with the variant on, against the oracle's 8-bit forward, with the bf16
+  tolerances of the other forward tests (the GPU's activations are bf16 where the
+  oracle's are fp64, so a few codes straddle a rounding boundary differently, and the
+  kernel's probability rounding is not modelled).  At the full 1.3B block, where the
+  quantisation moves the result well beyond bf16 rounding, the GPU result must also lie
+  closer to the oracle's 8-bit result than to the exact (unquantised) one: it computes
+  the 8-bit method, not the bf16 one.
 """
 import os
 
@@ -248,10 +250,9 @@ def test_tiny_forward_fp8_variant(wan, bits):
     ctx_o = O.text_projection(inp["text"], w)
     o8 = O.dit_forward(lat, t, ctx_o, None, w, s)
     ex = O.dit_forward(lat, t, ctx_o, None, w, s.replace(fp8=0))
-    e_gpu, e_q = _rel_rms(g, o8), _rel_rms(o8, ex)
-    _log(what=f"tiny fp8={bits}", kind="fp8_forward", gpu_vs_oracle8=e_gpu, oracle8_vs_exact=e_q, ok=bool(e_gpu <= e_q))
-    assert np.all(np.isfinite(g))
-    assert e_gpu <= e_q, f"fp8={bits}: |gpu - oracle8| {e_gpu:.3e} > |oracle8 - exact| {e_q:.3e}"
+    _log(what=f"tiny fp8={bits}", kind="fp8_forward", gpu_vs_oracle8=_rel_rms(g, o8), oracle8_vs_exact=_rel_rms(o8, ex),
+         ok=True)
+    assert_bf16_close(g, o8, f"tiny forward fp8={bits}")
 
 
 def test_wan13b_block_fp8_variant(wan):
@@ -273,5 +274,7 @@ def test_wan13b_block_fp8_variant(wan):
     e_gpu, e_q = _rel_rms(head, g8["head"]), _rel_rms(g8["head"], gx["head"])
     _log(what="wan1.3b-block fp8", kind="fp8_forward", gpu_vs_oracle8=e_gpu, oracle8_vs_exact=e_q,
          gpu_vs_exact=_rel_rms(head, gx["head"]), ok=bool(e_gpu <= e_q))
-    assert np.all(np.isfinite(head))
-    assert e_gpu <= e_q, f"|gpu - oracle8| {e_gpu:.3e} > |oracle8 - exact| {e_q:.3e}"
+    assert_bf16_close(head, g8["head"], "wan1.3b block fp8 head rows")
+    e_exact = _rel_rms(head, gx["head"])
+    assert e_gpu <= e_q and e_gpu < 0.5 * e_exact, \
+        f"|gpu - oracle8| {e_gpu:.3e}, |oracle8 - exact| {e_q:.3e}, |gpu - exact| {e_exact:.3e}"
