@@ -9,10 +9,10 @@
 //   warp 0      TMA: Q once, then K and V tiles into 2-deep rings
 //   warp 1      tcgen05.mma from one thread: S_i = Q_i K^T (both operands in smem),
 //               O_i += P_i V (P from TMEM, V tile from smem), ping-ponging the tiles.
-//               Per key tile j: PV_0(j); then S_0(j+1) and PV_1(j) interleaved MMA by
-//               MMA (the smem-bound SS product alternating with the TMEM-fed TS product
-//               keeps both operand paths busy); then S_1(j+1).  S_i(j+1) always follows
-//               PV_i(j), because P_i overwrites S_i in TMEM.
+//               Per key tile j: PV_0(j), S_0(j+1) | wait for P_1(j) | PV_1(j), S_1(j+1):
+//               each tile's cycle is its own MMAs plus its softmax, the two tiles half
+//               a cycle apart.  S_i(j+1) always follows PV_i(j), because P_i overwrites
+//               S_i in TMEM.
 //   warps 4..11 softmax, one warpgroup per query tile, one thread per query row: fp32
 //               running max and sum, exp2 on the MUFU unit, lazy rescale of O in TMEM
 //               only when the running max grows by more than 2^8, final 1/l and store.
@@ -51,7 +51,7 @@ struct AttnCfg {
   static constexpr int PRODUCER_REGS = 56;
   static constexpr int SOFTMAX_REGS = 224;
   static_assert(128 * PRODUCER_REGS + 256 * SOFTMAX_REGS <= 384 * 168, "register split");
-  static_assert(HD % 64 == 0 && HD <= BKV, "the interleaved S/PV issue assumes HD/16 <= BKV/16 K steps");
+  static_assert(HD % 64 == 0, "Q/K/V tiles are whole 64-column (128-byte) boxes");
 };
 
 struct AttnParams {
@@ -206,24 +206,17 @@ __global__ void __launch_bounds__(384, 1)
       if (more && !mbar_wait(&k_full[ks], ((j + 1) >> 1) & 1, status, kDevTimeoutAttn)) { ok = false; break; }
       if (!mbar_wait(&p_ready[0], j & 1, status, kDevTimeoutAttn)) { ok = false; break; }
       tc_fence_after();
+      // Tile 0's next scores right behind its PV product: its softmax starts as soon as
+      // they finish, independently of tile 1 (the tensor pipe runs them in order, so
+      // S_0(j+1) overwrites P_0 only after PV_0(j) has read it).
       issue_PV(0, vs, j > 0 ? 1u : 0u);
+      if (more) issue_S(0, ks);
+      tc_commit(&s_full[0]);
       if (ntile == 2) {
         if (!mbar_wait(&p_ready[1], j & 1, status, kDevTimeoutAttn)) { ok = false; break; }
         tc_fence_after();
-        // S_0(j+1) (both operands in smem) interleaved with PV_1(j) (A in TMEM).
-        const uint32_t va = vs ? v_lo1 : v_lo0;
-        const uint32_t ka = ks ? k_lo1 : k_lo0;
-#pragma unroll
-        for (int kk = 0; kk < Cfg::BKV / 16; ++kk) {  // PV: BKV/16 key steps; S: HD/16 <= BKV/16 steps
-          if (more && kk < HD / 16) {
-            const uint32_t off = ((kk >> 2) * Cfg::Q_BOX + (kk & 3) * 32) >> 4;
-            tc_mma_ss_lo(tmem_base, q_lo0 + off, ka + off, idS, kk > 0 ? 1u : 0u);
-          }
-          const uint32_t voff = (kk * 16 * 128) >> 4;
-          tc_mma_ts_lo(tmem_base + 256 + 128, tmem_base + 256 + kk * 8, va + voff, idO, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        issue_PV(1, vs, j > 0 ? 1u : 0u);
         tc_commit(&v_empty[vs]);
-        tc_commit(&s_full[0]);
         if (more) {
           issue_S(1, ks);
           tc_commit(&k_empty[ks]);
@@ -231,11 +224,7 @@ __global__ void __launch_bounds__(384, 1)
         tc_commit(&s_full[1]);
       } else {
         tc_commit(&v_empty[vs]);
-        if (more) {
-          issue_S(0, ks);
-          tc_commit(&k_empty[ks]);
-        }
-        tc_commit(&s_full[0]);
+        if (more) tc_commit(&k_empty[ks]);
       }
     }
     if (!ok) {

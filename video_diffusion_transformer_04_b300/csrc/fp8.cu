@@ -14,6 +14,8 @@
 // tiles per CTA, TMA / MMA / two softmax warpgroups, S and O of each tile in TMEM) on
 // 8-bit operands: S = Q8 K8^T and O += P8 V8 by tcgen05.mma kind::f8f6f4, K = 32 per
 // instruction, so each 128-key step takes half the MMA instructions of the bf16 kernel.
+// Issue order per key tile j: PV_0(j), S_0(j+1) | wait P_1(j) | PV_1(j), S_1(j+1): each
+// tile's cycle is its own MMAs plus its softmax, the two tiles half a cycle apart.
 // Softmax per row, fp32: the logit of key j is S_j * c with c = log2(e)/sqrt(d) * sq_row *
 // sk_block; P' = 2^(S_j c - m + 8) is rounded to E4M3 into TMEM (four keys per 32-bit
 // column) and the row sum accumulates the unrounded P'; O = (sum_j P'_j V8_j) * sv / l.
@@ -409,20 +411,17 @@ __global__ void __launch_bounds__(384, 1)
       if (more && !mbar_wait(&k_full[ks], ((j + 1) / ST) & 1, status, kDevTimeoutAttn8)) { ok = false; break; }
       if (!mbar_wait(&p_ready[0], j & 1, status, kDevTimeoutAttn8)) { ok = false; break; }
       tc_fence_after();
+      // Tile 0's next scores right behind its PV product: its softmax can start as soon
+      // as these finish, independently of tile 1 (the tensor pipe runs them in order, so
+      // S_0(j+1) overwrites P_0 only after PV_0(j) has read it).
       issue_PV(0, vs, j > 0 ? 1u : 0u);
+      if (more) issue_S(0, ks);
+      tc_commit(&s_full[0]);
       if (ntile == 2) {
         if (!mbar_wait(&p_ready[1], j & 1, status, kDevTimeoutAttn8)) { ok = false; break; }
         tc_fence_after();
-        // S_0(j+1) interleaved with PV_1(j), instruction by instruction.
-        const uint32_t va = v_lo0 + vs * kTileLo, ka = k_lo0 + ks * kTileLo;
-#pragma unroll
-        for (int kk = 0; kk < Cfg::BKV / 32; ++kk) {
-          if (more && kk < HD / 32) tc_mma_ss_f8_lo(tmem_base, q_lo0 + kk * 2, ka + kk * 2, idS, kk > 0 ? 1u : 0u);
-          tc_mma_ts_f8_lo(tmem_base + 256 + 128, tmem_base + 256 + kk * 8, va + kk * 2, idO,
-                          (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        issue_PV(1, vs, j > 0 ? 1u : 0u);
         tc_commit(&v_empty[vs]);
-        tc_commit(&s_full[0]);
         if (more) {
           issue_S(1, ks);
           tc_commit(&k_empty[ks]);
@@ -430,11 +429,7 @@ __global__ void __launch_bounds__(384, 1)
         tc_commit(&s_full[1]);
       } else {
         tc_commit(&v_empty[vs]);
-        if (more) {
-          issue_S(0, ks);
-          tc_commit(&k_empty[ks]);
-        }
-        tc_commit(&s_full[0]);
+        if (more) tc_commit(&k_empty[ks]);
       }
     }
     if (!ok) {
