@@ -10,6 +10,7 @@ kernels' outputs with these values at the stored positions.
     python tests/golden/make_goldens.py --workload wan14b-i2v-block            # one 14B I2V block
     python tests/golden/make_goldens.py --workload wan1.3b-20step-sampler      # 20 steps on a shrunk latent
     python tests/golden/make_goldens.py --workload wan1.3b-block --fp8 3       # the 8-bit variant of one block
+    python tests/golden/make_goldens.py --workload wan14b-i2v-block --fp8 3    # the same at the 14B I2V shape
 
 Outputs ``tests/golden/<workload>.npz`` (``-shrunk`` for the sampler, ``-fp8`` for the
 8-bit variant; float32 values, int64 indices).
