@@ -98,3 +98,47 @@ def test_dit_workspace_size_arithmetic():
     bad = wan.wan_dit_config(**{f: getattr(cfg, f) for f, _ in cfg._fields_})
     bad.head_dim, bad.heads = 96, 16
     assert wan.wan_dit_workspace_size(bad) == 0       # bf16 attention takes d = 64 or 128
+
+
+def test_host_validation_of_the_8bit_entry_points(wanlib):
+    P, I, LL, SZ = C.c_void_p, C.c_int, C.c_longlong, C.c_size_t
+    A = 1 << 12  # a 16-byte-aligned dummy address: only reached by the host checks
+    q = wanlib.wan_quant_rows_e4m3
+    q.argtypes = [P, I, LL, I, I, P, LL, P, P]
+    assert q(None, 0, 64, 8, 64, A, 64, A, None) == -1           # NULL x
+    assert q(A, 7, 64, 8, 64, A, 64, A, None) == -1              # unknown dtype
+    assert q(A, 0, 64, 8, 62, A, 64, A, None) == -2              # K % 4
+    qa = wanlib.wan_quant_attn_e4m3
+    qa.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, SZ, P]
+    args = [A, A, A, 2, 0, 1, 300, 2, 128, A, A, A, A, A, A]
+    assert qa(*args, A, 1 << 20, None) != -1                      # well-formed (fails later, no GPU)
+    assert qa(None, *args[1:], A, 1 << 20, None) == -1           # NULL q
+    assert qa(*args[:3], 1, *args[4:], A, 1 << 20, None) == -1   # fp32 q/k are not a quantiser input
+    assert qa(*args[:8], 64, *args[9:], A, 1 << 20, None) == -2  # d must be 128
+    assert qa(*args, None, 0, None) == -5                        # no workspace
+    assert qa(*args, A, 16, None) == -5                          # too small (needs B*H*d*4)
+    at = wanlib.wan_attn_e4m3
+    at.argtypes = [P] * 8 + [I] * 4 + [P]
+    assert at(None, A, A, A, A, A, A, None, 1, 300, 2, 128, None) == -1
+    assert at(A, A, A, A, A, A, A, None, 1, 300, 2, 64, None) == -2
+    li = wanlib.wan_linear_e4m3
+    li.argtypes = [P] * 6 + [I] * 4 + [P, I, P]
+    assert li(None, A, A, A, None, A, 8, 64, 64, 0, None, 0, None) == -1
+    assert li(A, A, A, A, None, A, 8, 64, 64, 9, None, 0, None) == -1   # unknown epilogue
+    assert li(A, A, A, A, None, A, 8, 48, 64, 0, None, 0, None) == -2   # N % 32
+    assert li(A, A, A, A, None, A, 8, 64, 56, 0, None, 0, None) == -2   # K % 16
+
+
+def test_dit_workspace_size_of_the_8bit_variant():
+    from video_diffusion_transformer_04_b300 import wan
+    base = dict(dtype=wan.WAN_BF16, batch=2, c_in=16, c_out=16, frames=21, height=60, width=104, dim=1536,
+                heads=12, head_dim=128, ffn=8960, blocks=30, text_len=512, img_len=0, freq_dim=256,
+                theta=10000.0, eps=1e-6)
+    n0 = wan.wan_dit_workspace_size(wan.wan_dit_config(**base))
+    n3 = wan.wan_dit_workspace_size(wan.wan_dit_config(**base, fp8=3))
+    M, D, H, d, L = 2 * 32760, 1536, 12, 128, 32760
+    # y8 + sy, q8 + k8, v8t (+ scales): at least 4 M*D bytes more
+    assert n3 - n0 >= 4 * M * D and n3 - n0 <= 4 * M * D + 16 * M * H + (1 << 20)
+    assert wan.wan_dit_workspace_size(wan.wan_dit_config(**base, fp8=4)) == 0
+    assert wan.wan_dit_workspace_size(wan.wan_dit_config(**dict(base, dtype=wan.WAN_F32), fp8=1)) == 0
+    assert wan.wan_dit_workspace_size(wan.wan_dit_config(**dict(base, heads=24, head_dim=64), fp8=1)) == 0

@@ -778,7 +778,8 @@ int wan_quant_attn_e4m3(const void* q, const void* k, const void* v, int qk_dtyp
   const void* ptrs[] = {q, k, v, q8, k8, v8t};
   for (const void* p : ptrs)
     if (!aligned16(p)) return WAN_ERR_UNSUPPORTED;
-  if (!ws || ws_bytes < wan_quant_attn_workspace_size(B, H, d)) return WAN_ERR_WORKSPACE;
+  if (!ws || ws_bytes < wan_quant_attn_workspace_size(B, H, d) || (reinterpret_cast<uintptr_t>(ws) & 3))
+    return WAN_ERR_WORKSPACE;
   LaunchCtx c;
   WAN_TRY(launch_ctx(stream, &c));
   Attn8Operands a;
