@@ -32,9 +32,9 @@ named where it is used (READING: ...).
 
 Parity pins: every function here is checked by tests/test_oracle_pins.py
 against closed forms, brute force, invariants and special cases.  The full
-composition (``dit_forward`` over 30 blocks, ``sample``) has no printed worked
-example: beyond the pins of its parts and the zero-gate identity it is
-"parity unpinned".
+composition (``dit_forward`` over 30 blocks, ``sample``, and the 8-bit block)
+has no printed worked example: beyond the pins of its parts and the zero-gate
+identity it is "parity unpinned".
 """
 from __future__ import annotations
 
