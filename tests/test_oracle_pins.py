@@ -635,3 +635,114 @@ def test_fp8_block_variant_close_to_exact_and_zero_gates_reduce_to_exact():
     mods0 = mods.copy(); mods0[2] = 0.0; mods0[5] = 0.0
     y0 = O.dit_block(x, mods0, blk, ctx, None, O.Hyper.of(s.replace(fp8=3)))
     assert np.allclose(y0, O.dit_block(x, mods0, blk, ctx, None, O.Hyper.of(s)), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- cross-attention and head
+
+def _cross_weights(D, rng_, **over):
+    blk = {"cq_w": rng_.normal(size=(D, D)) * 0.3, "cq_b": rng_.normal(size=D) * 0.1,
+           "ckv_w": rng_.normal(size=(2 * D, D)) * 0.3, "ckv_b": rng_.normal(size=2 * D) * 0.1,
+           "co_w": rng_.normal(size=(D, D)) * 0.3, "co_b": rng_.normal(size=D) * 0.1}
+    blk.update(over)
+    return blk
+
+
+def test_cross_attention_single_text_token_is_its_value_projection():
+    # One key: every softmax row is exactly 1, so each output row is the output projection
+    # of that token's value half (rows D..2D of the key/value projection), whatever x is.
+    # A swap of the key and value halves, a dropped bias or a missing output projection
+    # changes the result.
+    D, H = 12, 3
+    r = np.random.default_rng(7)
+    blk = _cross_weights(D, r)
+    hp = O.Hyper(D, H, (1, 1, 1))
+    ctx = r.normal(size=(1, D))
+    x = r.normal(size=(5, D)) * 2.0
+    v = np.array([sum(blk["ckv_w"][D + n, c] * ctx[0, c] for c in range(D)) + blk["ckv_b"][D + n]
+                  for n in range(D)])
+    expect = np.array([sum(blk["co_w"][n, c] * v[c] for c in range(D)) + blk["co_b"][n] for n in range(D)])
+    out = O.cross_attention(x, blk, ctx, None, hp)
+    assert np.allclose(out, np.broadcast_to(expect, out.shape), atol=1e-12)
+
+
+def test_cross_attention_two_keys_logistic_closed_form():
+    # Two text tokens, a query fixed by the bias (cq_w = 0), identity value and output
+    # projections: per head, the output is sigmoid(z) v0 + sigmoid(-z) v1 with
+    # z = q_h . (k0_h - k1_h) / sqrt(d).  Pins which half of ckv_w makes keys, the
+    # 1/sqrt(d) scale, and that heads do not mix.
+    D, H = 8, 2
+    d = D // H
+    r = np.random.default_rng(11)
+    q = np.array([0.5, -1.0, 0.25, 2.0, -0.75, 0.5, 1.5, -0.25])
+    Wk = r.normal(size=(D, D))
+    blk = {"cq_w": np.zeros((D, D)), "cq_b": q,
+           "ckv_w": np.concatenate([Wk, np.eye(D)]), "ckv_b": np.zeros(2 * D),
+           "co_w": np.eye(D), "co_b": np.zeros(D)}
+    ctx = r.normal(size=(2, D))
+    k = ctx @ Wk.T
+    expect = np.empty(D)
+    for h in range(H):
+        sl = slice(h * d, (h + 1) * d)
+        z = float(q[sl] @ (k[0, sl] - k[1, sl])) / math.sqrt(d)
+        p0 = 1.0 / (1.0 + math.exp(-z))
+        expect[sl] = p0 * ctx[0, sl] + (1.0 - p0) * ctx[1, sl]
+    out = O.cross_attention(r.normal(size=(3, D)), blk, ctx, None, O.Hyper(D, H, (1, 1, 1)))
+    assert np.allclose(out, np.broadcast_to(expect, out.shape), atol=1e-13)
+
+
+def test_cross_attention_query_layer_norm():
+    # The query passes through a LayerNorm: a positive scale and a constant shift of each
+    # row of x leave the output unchanged (up to eps), while a change of x's shape does not.
+    D, H = 16, 4
+    r = np.random.default_rng(13)
+    blk = _cross_weights(D, r)
+    hp = O.Hyper(D, H, (1, 1, 1))
+    ctx = r.normal(size=(6, D))
+    x = r.normal(size=(4, D))
+    a = np.array([3.0, 0.5, 7.0, 1.5])[:, None]
+    c = np.array([10.0, -4.0, 0.25, 100.0])[:, None]
+    out = O.cross_attention(x, blk, ctx, None, hp)
+    assert np.allclose(O.cross_attention(a * x + c, blk, ctx, None, hp), out, atol=1e-6)
+    assert not np.allclose(O.cross_attention(x ** 3, blk, ctx, None, hp), out, atol=1e-3)
+
+
+def test_cross_attention_decoupled_one_token_each_is_sum_of_values():
+    # One text and one image token: two separate softmaxes (each exactly 1), so the output
+    # is the output projection of v_text + v_image; one joint softmax over the
+    # concatenated context would average them instead.
+    D, H = 8, 2
+    r = np.random.default_rng(17)
+    blk = _cross_weights(D, r)
+    blk["ckvi_w"], blk["ckvi_b"] = r.normal(size=(2 * D, D)), r.normal(size=2 * D)
+    ct, ci = r.normal(size=(1, D)), r.normal(size=(1, D))
+    vt = blk["ckv_w"][D:] @ ct[0] + blk["ckv_b"][D:]
+    vi = blk["ckvi_w"][D:] @ ci[0] + blk["ckvi_b"][D:]
+    expect = blk["co_w"] @ (vt + vi) + blk["co_b"]
+    out = O.cross_attention(r.normal(size=(3, D)), blk, ct, ci, O.Hyper(D, H, (1, 1, 1)))
+    assert np.allclose(out, np.broadcast_to(expect, out.shape), atol=1e-12)
+
+
+def test_head_layer_norm_modulation_and_projection_closed_form():
+    # Rows [a+b, a-b, a+b, a-b] have mean a and variance b^2, so LN gives
+    # [1, -1, 1, -1] * b / sqrt(b^2 + eps).  With (shift, scale) = hm and a 4-cycle
+    # permutation as the projection, each output is LN * (1 + scale) + shift at the
+    # permuted index plus the bias: a swapped shift/scale, a transposed weight or a
+    # missing LN changes it.
+    eps = 1e-6
+    x = np.array([[3.0 + 2.0, 3.0 - 2.0, 3.0 + 2.0, 3.0 - 2.0],
+                  [-1.0 + 0.5, -1.0 - 0.5, -1.0 + 0.5, -1.0 - 0.5]])
+    bs = np.array([2.0, 0.5])
+    shift = np.array([0.1, -0.2, 0.3, 0.05])
+    scale = np.array([1.0, 0.0, -0.5, 2.0])
+    perm = [1, 2, 3, 0]  # output n reads modulated feature perm[n]
+    w = {"head_w": np.eye(4)[perm], "head_b": np.array([0.01, 0.02, 0.03, 0.04])}
+    out = O.head(x, np.stack([shift, scale]), w, eps)
+    sign = np.array([1.0, -1.0, 1.0, -1.0])
+    for r_ in range(2):
+        ln = sign * bs[r_] / math.sqrt(bs[r_] ** 2 + eps)
+        mod = ln * (1.0 + scale) + shift
+        assert np.allclose(out[r_], [mod[perm[n]] + w["head_b"][n] for n in range(4)], atol=1e-14)
+    # zero modulation and identity projection: the head is the plain LayerNorm
+    w0 = {"head_w": np.eye(4), "head_b": np.zeros(4)}
+    out0 = O.head(x, np.zeros((2, 4)), w0, eps)
+    assert np.allclose(out0[0], sign * 2.0 / math.sqrt(4.0 + eps), atol=1e-15)
