@@ -230,8 +230,10 @@ int wan_text_embed(const void* text, const void* w1, const void* b1, const void*
  *   - Sizes whose scratch, wan_text_embed_workspace_size(B, Lt, D, dtype), exceeds the
  *     maximum are rejected with WAN_ERR_WORKSPACE before anything is launched (bf16: up
  *     to B*Lt*D = 8 Mi elements).
- *   - The first call on a device resolves the array's device address (once per device);
- *     make that first call before capturing a stream into a CUDA graph.
+ *   - Every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress, no allocation); the first lookup on a device may load the
+ *     library's module there, so make the first call on each device outside stream
+ *     capture.
  *   - Every call on a device shares the one array, which keeps the last call's contents
  *     (the scratch is fully written before it is read, so nothing needs clearing).
  *     Calls whose work overlaps on the GPU (different streams, concurrent graphs) race on

@@ -57,9 +57,19 @@ def f32_error(g, o):
     return float(np.max(np.abs(g - o) / np.maximum(np.abs(o), rms)))
 
 
+def f32_error_unfloored(g, o):
+    """max_i |g_i - o_i| / |o_i| over the elements with o_i != 0 (no RMS floor)."""
+    g = np.asarray(g, np.float64)
+    o = np.asarray(o, np.float64)
+    nz = o != 0
+    if not np.any(nz):
+        return 0.0
+    return float(np.max(np.abs(g[nz] - o[nz]) / np.abs(o[nz])))
+
+
 def assert_f32_close(g, o, what="", tol=F32_MAX_REL):
     e = f32_error(g, o)
-    _log(what=what, kind="f32", max_rel=e, tol=tol, ok=bool(e <= tol))
+    _log(what=what, kind="f32", max_rel=e, max_rel_unfloored=f32_error_unfloored(g, o), tol=tol, ok=bool(e <= tol))
     assert e <= tol, f"{what}: max rel err {e:.3e} > {tol}"
     return e
 

@@ -76,6 +76,17 @@ int launch_ctx(cudaStream_t stream, LaunchCtx* ctx) {
   return WAN_OK;
 }
 
+int set_smem_limit_once(const void* func, int bytes, std::atomic<unsigned long long>* done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WAN_ERR_CUDA;
+  const unsigned long long bit = 1ull << dev;
+  if (done->load(std::memory_order_acquire) & bit) return WAN_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return WAN_ERR_CUDA;
+  done->fetch_or(bit, std::memory_order_release);  // racing threads set the same value
+  return WAN_OK;
+}
+
 // ------------------------------------------------------------------ tensor maps
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 static std::once_flag g_encode_once;

@@ -394,12 +394,10 @@ template <int HD, bool QK_F16>
 static int launch_attn(const LaunchCtx& c, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const AttnParams& p, int B, const char* tag) {
   using Cfg = AttnCfg<HD>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_bf16_tc_kernel<HD, QK_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::SMEM) != cudaSuccess)
-      return WAN_ERR_CUDA;
-    attr_set = true;
+  static std::atomic<unsigned long long> smem_set{0};
+  {
+    const int st = set_smem_limit_once(reinterpret_cast<const void*>(attn_bf16_tc_kernel<HD, QK_F16>), Cfg::SMEM, &smem_set);
+    if (st != WAN_OK) return st;
   }
   const long long grid = (long long)B * p.H * p.nq_pairs;
   count_launch(tag, c.stream, true);

@@ -658,12 +658,10 @@ int attention_e4m3(const LaunchCtx& c, const Attn8Args& a) {
   p.ldo = a.ldo;
   p.o_col = a.o_col;
   p.kv_lens = a.kv_lens;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_e4m3_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
-        cudaSuccess)
-      return WAN_ERR_CUDA;
-    attr_set = true;
+  static std::atomic<unsigned long long> smem_set{0};
+  {
+    const int st = set_smem_limit_once(reinterpret_cast<const void*>(attn_e4m3_tc_kernel<128>), Cfg::SMEM, &smem_set);
+    if (st != WAN_OK) return st;
   }
   const long long grid = (long long)a.B * a.H * p.nq_pairs;
   const char* tag = a.tag ? a.tag : "attn_e4m3";

@@ -244,12 +244,10 @@ template <int BN, bool FP8>
 static int launch_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr,
                        const EpiParams& ep, int M, int N, int K, int kb_period, const char* tag) {
   using Cfg = GemmCfg<BN>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<BN, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
-        cudaSuccess)
-      return WAN_ERR_CUDA;
-    attr_set = true;
+  static std::atomic<unsigned long long> smem_set{0};
+  {
+    const int st = set_smem_limit_once(reinterpret_cast<const void*>(gemm_bf16_tc_kernel<BN, FP8>), Cfg::SMEM, &smem_set);
+    if (st != WAN_OK) return st;
   }
   const int tiles = ((M + 127) / 128) * ((N + BN - 1) / BN);
   const int grid = tiles < c.num_sms ? tiles : c.num_sms;

@@ -1,10 +1,18 @@
 // Internal interface between the kernel files and the C-ABI layer (api.cu).
 #pragma once
 
+#include <atomic>
+
 #include "epilogue.cuh"
 #include "wan_common.cuh"
 
 namespace wan {
+
+// ------------------------------------------------------------------ launch attributes (api.cu)
+// Raise `func`'s dynamic shared-memory limit to `bytes` on the current device.  The
+// attribute belongs to the device that is current when it is set, so `done` keeps one
+// bit per device ordinal (0..63) and the call is made once per device.
+int set_smem_limit_once(const void* func, int bytes, std::atomic<unsigned long long>* done);
 
 // ------------------------------------------------------------------ tensor maps (api.cu)
 // 2D / 3D tiled maps with 128-byte swizzle and zero fill outside the tensor.

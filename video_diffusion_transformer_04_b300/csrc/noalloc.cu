@@ -8,8 +8,6 @@
 // point keeps the projection's scratch (the hidden activations between the two linear
 // layers) in a statically sized device array that lives in this library's module for as
 // long as the process has the library loaded on that device.
-#include <mutex>
-
 #include "kernels.h"
 
 namespace wan {
@@ -25,22 +23,14 @@ static __device__ __align__(256) unsigned char g_text_embed_scratch[wan::kTextEm
 
 namespace {
 
-std::mutex g_mu;
-void* g_scratch_addr[64] = {};  // device address of g_text_embed_scratch, per device
-
-// Resolve the device address of the scratch array on the current device (once per
-// device).  In host code the array's name is only a host-side stand-in, so the kernels
-// receive this address instead.
+// Device address of the scratch array on the current device.  In host code the array's
+// name is only a host-side stand-in, so the kernels receive this address instead.  It is
+// looked up on every call (cheap): an address cached per device ordinal would go stale
+// if the caller reset the device and loaded the module again.
 int scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WAN_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_text_embed_scratch) != cudaSuccess || p == nullptr) return WAN_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_text_embed_scratch) != cudaSuccess || p == nullptr) return WAN_ERR_CUDA;
+  *out = p;
   return WAN_OK;
 }
 
