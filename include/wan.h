@@ -59,7 +59,9 @@ enum wan_status_code {
 
 /* Storage types.  WAN_F16 (fp16) is accepted only where an entry point says so: for the
  * q and k operands of the attention calls next to bf16 v and o (fp16 keeps 3 more
- * mantissa bits in the logits q.k than bf16), and as the output of wan_linear. */
+ * mantissa bits in the logits q.k than bf16), for the whole cross-attention sub-layer
+ * (wan_adaln_modulate's output, wan_linear's operands and output, wan_cross_attn's v and
+ * o), and as the output of wan_linear. */
 enum wan_dtype { WAN_BF16 = 0, WAN_F32 = 1, WAN_F16 = 2 };
 
 /* Epilogues of wan_linear: y = x W^T + b followed by ... */
@@ -103,7 +105,9 @@ int wan_patchify(const float* latent, const void* w, const void* b, float* x, in
 /* ------------------------------------------------------------------ AdaLN
  * [Code] DiT-style modulation: y = LN(x) * (1 + scale[b]) + shift[b], LN over D with
  * biased variance, no affine, epsilon eps.  x: fp32 [B, L, D]; shift, scale: fp32 [B, D]
- * (both NULL: plain LN).  y: [B, L, D] in dtype.  Needs D % 4 == 0, D <= 8192. */
+ * (both NULL: plain LN).  y: [B, L, D] in dtype (WAN_BF16, WAN_F16 or WAN_F32; fp16 is
+ * meant for the unmodulated LN of the cross-attention query, whose rows have norm
+ * sqrt(D)).  Needs D % 4 == 0, D <= 8192. */
 int wan_adaln_modulate(const float* x, const float* shift, const float* scale, void* y, int B, int L,
                        int D, float eps, int dtype, wan_stream_t stream);
 
@@ -132,10 +136,13 @@ int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, const 
 /* ------------------------------------------------------------------ cross-attention
  * [Method] text conditioning by cross-attention; [I2V] decoupled cross-attention to the
  * CLIP image context: o = softmax(q kt^T/sqrt(d)) vt + softmax(q ki^T/sqrt(d)) vi
- * (the second term only when ki != NULL).
- * o: [B, L, H, d]; vt: [B, Lt, H, d]; vi: [B, Li, H, d] or NULL (dtype).
+ * (the second term only when ki != NULL).  Both softmaxes run in one launch; the two
+ * terms are summed in fp32 and rounded once (in the 16-bit formats the text term is
+ * parked in o between the two segments, so it is rounded to o's type once more).
+ * o: [B, L, H, d]; vt: [B, Lt, H, d]; vi: [B, Li, H, d] or NULL (dtype: WAN_BF16, WAN_F16
+ * or WAN_F32).
  * q: [B, L, H, d]; kt: [B, Lt, H, d]; ki: [B, Li, H, d] or NULL (qk_dtype: dtype, or
- * WAN_F16 with dtype WAN_BF16).
+ * WAN_F16 with dtype WAN_BF16; WAN_F16 with dtype WAN_F16).
  * kt_lens: DEVICE int [B] or NULL: valid text tokens per entry of a padded context (the
  * k_lens of [Code]; clamped to [1, Lt]; padded keys must be finite); the image segment
  * is always fully valid.
@@ -157,9 +164,10 @@ int wan_ffn(const void* y, const void* w1, const void* b1, const void* w2, const
 
 /* ------------------------------------------------------------------ linear
  * One projection y = x W^T + b with an epilogue (enum wan_epilogue); the GEMM under every
- * projection of the block.  x: [M, K] (dtype); w: [N, K]; b: [N] or NULL (dtype).
+ * projection of the block.  x: [M, K] and w: [N, K] in dtype (WAN_BF16, WAN_F16 or
+ * WAN_F32; x and w share it); b: [N] or NULL (bf16 with the 16-bit dtypes, else fp32).
  * WAN_EPI_STORE / WAN_EPI_GELU write out [M, N] in out_dtype (WAN_BF16 or WAN_F16 only
- * with dtype WAN_BF16).  WAN_EPI_RESIDUAL accumulates into the fp32 out [M, N] with the
+ * with a 16-bit dtype).  WAN_EPI_RESIDUAL accumulates into the fp32 out [M, N] with the
  * optional fp32 gate [M / rows_per_gate, N] (out_dtype WAN_F32).  Needs K % 8 == 0,
  * N % 32 == 0. */
 int wan_linear(const void* x, const void* w, const void* b, void* out, int M, int N, int K,
@@ -253,6 +261,12 @@ int wan_cfg_euler_step(float* x, const void* v_cond, const void* v_uncond, long 
                        float guide_scale, float dt, int v_dtype, wan_stream_t stream);
 
 /* ------------------------------------------------------------------ whole DiT forward */
+/* With dtype WAN_BF16 the cross-attention sub-layer runs in fp16 storage: its LN output,
+ * q, k, v, probabilities and o, and therefore its two square weights cq_w and co_w, which
+ * the caller stores in fp16 (every other weight, bias and activation is bf16).  Its
+ * values are bounded (an unmodulated LN row has norm sqrt(D); the probabilities stay
+ * below 2^15), and fp16's 3 extra mantissa bits keep the error of wide models' peaked
+ * softmaxes at the level of the narrow ones. */
 typedef struct wan_dit_config {
   int dtype;       /* WAN_BF16 or WAN_F32 */
   int batch;       /* B */
@@ -280,10 +294,10 @@ typedef struct wan_block_weights {
   const void* mod;                  /* [6, D]  learned bias added to the shared e0 */
   const void *qkv_w, *qkv_b;        /* [3D, D], [3D] */
   const void *o_w, *o_b;            /* [D, D], [D] */
-  const void *cq_w, *cq_b;          /* [D, D], [D]   cross-attention query */
+  const void *cq_w, *cq_b;          /* [D, D], [D]   cross-attention query (cq_w fp16 with WAN_BF16) */
   const void *ckv_w, *ckv_b;        /* [2D, D], [2D] text key|value */
   const void *ckvi_w, *ckvi_b;      /* [2D, D], [2D] image key|value (NULL when img_len == 0) */
-  const void *co_w, *co_b;          /* [D, D], [D]   cross-attention output */
+  const void *co_w, *co_b;          /* [D, D], [D]   cross-attention output (co_w fp16 with WAN_BF16) */
   const void *f1_w, *f1_b;          /* [F, D], [F] */
   const void *f2_w, *f2_b;          /* [D, F], [D] */
   const void *norm_q_w, *norm_k_w;  /* [D], [D] RMSNorm weights (only with qk_norm) */

@@ -64,9 +64,12 @@ def test_block_composed_from_ops(wan, name):
     wan.wan_linear(o.view(L, D), blk["o_w"], blk["o_b"], x.view(L, D), wan.WAN_EPI_RESIDUAL, g1, L)
     check("x_sa", x)
 
-    wan.wan_adaln_modulate(x, None, None, y)
+    # The cross-attention sub-layer in fp16 storage, as the fused forward runs it: LN
+    # output, q, k, v, o and the query / output projection weights.
+    y16 = torch.empty(1, L, D, dtype=F16, device=dev)
+    wan.wan_adaln_modulate(x, None, None, y16)
     qc = torch.empty(1, L, H, d, dtype=F16, device=dev)
-    wan.wan_linear(y.view(L, D), blk["cq_w"], blk["cq_b"], qc.view(L, D))
+    wan.wan_linear(y16.view(L, D), blk["cq_w"], blk["cq_b"], qc.view(L, D))
     if s.text_dim:
         ctx = m.text_embed(to_dev(inp["text"], BF))
     else:
@@ -75,7 +78,7 @@ def test_block_composed_from_ops(wan, name):
 
     def kv_of(c, wname, bname, Lk):
         kb = torch.empty(1, Lk, H, d, dtype=F16, device=dev)
-        vb = torch.empty(1, Lk, H, d, dtype=BF, device=dev)
+        vb = torch.empty(1, Lk, H, d, dtype=F16, device=dev)
         wan.wan_linear(c.view(Lk, D), blk[wname][:D], blk[bname][:D], kb.view(Lk, D))
         wan.wan_linear(c.view(Lk, D), blk[wname][D:], blk[bname][D:], vb.view(Lk, D))
         return kb, vb
@@ -84,11 +87,8 @@ def test_block_composed_from_ops(wan, name):
     ki = vi = None
     if s.img_len:
         ki, vi = kv_of(to_dev(inp["ctx_img"][:1], BF), "ckvi_w", "ckvi_b", s.img_len)
-    cws = torch.empty(wan.wan_cross_attn_workspace_size(1, Lt, s.img_len, H, d, wan.WAN_BF16) + 1024,
-                      dtype=torch.uint8, device=dev)
-    cws = cws[(-cws.data_ptr()) % 1024:]
-    oc = torch.empty(1, L, H, d, dtype=BF, device=dev)
-    wan.wan_cross_attn(qc, kt, vt, ki, vi, oc, cws)
+    oc = torch.empty(1, L, H, d, dtype=F16, device=dev)
+    wan.wan_cross_attn(qc, kt, vt, ki, vi, oc)
     wan.wan_linear(oc.view(L, D), blk["co_w"], blk["co_b"], x.view(L, D), wan.WAN_EPI_RESIDUAL)
     check("x_ca", x)
 

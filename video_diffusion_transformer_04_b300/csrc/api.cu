@@ -168,12 +168,13 @@ static EpiParams epi_base(int kind, int M, int N, int rows_per_batch, const void
   return e;
 }
 
-// y = A W^T (+ epilogue) in the call's dtype.
+// y = A W^T (+ epilogue) in the call's dtype (fp32 SIMT, or 16-bit tensor cores with A
+// and W both bf16, or both fp16 when ab_f16).
 static int proj(const LaunchCtx& c, int f32, const void* A, long long lda, int a_cols, const void* W, long long ldw,
-                int w_cols, int M, int N, int K, int kb_period, const EpiParams& ep, const char* tag) {
+                int w_cols, int M, int N, int K, int kb_period, const EpiParams& ep, const char* tag,
+                bool ab_f16 = false) {
   if (f32) return gemm_f32(c, static_cast<const float*>(A), lda, static_cast<const float*>(W), ldw, M, N, K, ep, tag);
-  return gemm_bf16(c, static_cast<const bf16*>(A), lda, a_cols, static_cast<const bf16*>(W), ldw, w_cols, M, N, K,
-                   kb_period, ep, tag);
+  return gemm_bf16(c, A, lda, a_cols, W, ldw, w_cols, M, N, K, kb_period, ep, tag, ab_f16);
 }
 
 static int attend(const LaunchCtx& c, int f32, const AttnArgs& a) {
@@ -345,7 +346,7 @@ static int cross_kv_impl(const LaunchCtx& c, const wan_dit_config* cfg, const wa
     ep.ldo = 2LL * D;
     ep.out_type = f32 ? OUT_F32 : OUT_BF16;
     ep.n_rot = 0;
-    ep.n_f16 = f32 ? 0 : D;  // k in fp16, v in bf16
+    ep.n_f16 = f32 ? 0 : 2 * D;  // k and v in fp16: the cross-attention sub-layer computes in fp16
     ep.head_dim = cfg->head_dim;
     WAN_TRY(proj(c, f32, seg ? ctx_img : ctx_txt, D, D, seg ? bw.ckvi_w : bw.ckv_w, D, D, B * Lk, 2 * D, D, 0, ep,
                  "gemm_cross_kv"));
@@ -400,7 +401,7 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
     if (fp8_gemm)
       WAN_TRY(launch_ln_mod_e4m3(c, W.x, mod + 0 * D, mod + 1 * D, 6LL * D, W.y8, W.sy, M, L, D, cfg->eps));
     else
-      WAN_TRY(launch_ln_mod(c, W.x, mod + 0 * D, mod + 1 * D, 6LL * D, W.y, f32, M, L, D, cfg->eps));
+      WAN_TRY(launch_ln_mod(c, W.x, mod + 0 * D, mod + 1 * D, 6LL * D, W.y, f32 ? OUT_F32 : OUT_BF16, M, L, D, cfg->eps));
     {
       EpiParams ep = epi_base(EPI_QKV, M, 3 * D, L, bw.qkv_b, f32);
       ep.out = W.qkv;
@@ -457,14 +458,18 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
       WAN_TRY(proj(c, f32, W.o, D, D, bw.o_w, D, D, M, D, D, 0, ep, "gemm_o_gate"));
     }
 
-    // --- cross-attention: q = LN(x) Wq^T; k,v from the context; x += o Wo^T + bo
-    WAN_TRY(launch_ln_mod(c, W.x, nullptr, nullptr, 0, W.y, f32, M, L, D, cfg->eps));
+    // --- cross-attention: q = LN(x) Wq^T; k,v from the context; x += o Wo^T + bo.
+    // 16-bit path: the whole sub-layer runs in fp16 storage (LN output, q, k, v, the
+    // probabilities, o, and the weights cq_w / co_w): its values are bounded (an
+    // unmodulated LN row has norm sqrt(D); probabilities stay below 2^15), and fp16's 3
+    // extra mantissa bits cut the error of the peaked softmaxes of wide models.
+    WAN_TRY(launch_ln_mod(c, W.x, nullptr, nullptr, 0, W.y, f32 ? OUT_F32 : OUT_F16, M, L, D, cfg->eps));
     {
       EpiParams ep = epi_base(EPI_STORE, M, D, L, bw.cq_b, f32);
       ep.out = W.qc;
       ep.ldo = D;
       ep.out_type = f32 ? OUT_F32 : OUT_F16;
-      WAN_TRY(proj(c, f32, W.y, D, D, bw.cq_w, D, D, M, D, D, 0, ep, "gemm_cross_q"));
+      WAN_TRY(proj(c, f32, W.y, D, D, bw.cq_w, D, D, M, D, D, 0, ep, "gemm_cross_q", true));
     }
     void* kv_txt = W.kvc;
     void* kv_img = W.kvci;
@@ -474,34 +479,52 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
     } else {
       WAN_TRY(cross_kv_impl(c, cfg, bw, ctx_txt, ctx_img, kv_txt, kv_img));
     }
-    for (int seg = 0; seg < (Li ? 2 : 1); ++seg) {
-      const int Lk = seg ? Li : Lt;
-      void* kv = seg ? kv_img : kv_txt;
-      AttnArgs a;
+    if (f32) {
+      for (int seg = 0; seg < (Li ? 2 : 1); ++seg) {
+        const int Lk = seg ? Li : Lt;
+        void* kv = seg ? kv_img : kv_txt;
+        AttnArgs a;
+        memset(&a, 0, sizeof(a));
+        a.q = W.qc; a.ldq = D; a.q_row_len = D; a.q_col = 0;
+        a.k = kv; a.ldk = 2LL * D; a.k_row_len = 2 * D; a.k_col = 0;
+        a.v = kv; a.ldv = 2LL * D; a.v_row_len = 2 * D; a.v_col = D;
+        a.o = W.o; a.ldo = D; a.o_col = 0;
+        a.B = B; a.Lq = L; a.Lkv = Lk; a.H = H; a.head_dim = hd;
+        a.accumulate = seg;
+        a.kv_lens = seg ? nullptr : txt_lens;  // text keys may be padded; the image tokens are all valid
+        a.tag = "attn_cross";
+        WAN_TRY(attention_f32(c, a));
+      }
+    } else {
+      CrossArgs a;
       memset(&a, 0, sizeof(a));
       a.q = W.qc; a.ldq = D; a.q_row_len = D; a.q_col = 0;
-      a.k = kv; a.ldk = 2LL * D; a.k_row_len = 2 * D; a.k_col = 0;
-      a.v = kv; a.ldv = 2LL * D; a.v_row_len = 2 * D; a.v_col = D;
+      a.kt = kv_txt; a.vt = kv_txt; a.ldkt = a.ldvt = 2LL * D; a.kt_row_len = a.vt_row_len = 2 * D;
+      a.kt_col = 0; a.vt_col = D;
+      if (Li) {
+        a.ki = kv_img; a.vi = kv_img; a.ldki = a.ldvi = 2LL * D; a.ki_row_len = a.vi_row_len = 2 * D;
+        a.ki_col = 0; a.vi_col = D;
+      }
       a.o = W.o; a.ldo = D; a.o_col = 0;
-      a.B = B; a.Lq = L; a.Lkv = Lk; a.H = H; a.head_dim = hd;
-      a.accumulate = seg;
-      a.kv_lens = seg ? nullptr : txt_lens;  // text keys may be padded; the 257 image tokens are all valid
+      a.B = B; a.L = L; a.Lt = Lt; a.Li = Li; a.H = H; a.head_dim = hd;
+      a.kt_lens = txt_lens;  // text keys may be padded; the image tokens are all valid
+      a.qk_f16 = 1;
+      a.pv_f16 = 1;
       a.tag = "attn_cross";
-      a.qk_f16 = !f32;
-      WAN_TRY(attend(c, f32, a));
+      WAN_TRY(cross_attention_tc(c, a));
     }
     {
       EpiParams ep = epi_base(EPI_RESID, M, D, L, bw.co_b, f32);
       ep.resid = W.x;
       ep.ldr = D;
-      WAN_TRY(proj(c, f32, W.o, D, D, bw.co_w, D, D, M, D, D, 0, ep, "gemm_cross_o"));
+      WAN_TRY(proj(c, f32, W.o, D, D, bw.co_w, D, D, M, D, D, 0, ep, "gemm_cross_o", true));
     }
 
     // --- FFN: y = LN(x)(1+sc2)+sh2; h = GELU(y W1^T + b1); x += g2 (h W2^T + b2)
     if (fp8_gemm)
       WAN_TRY(launch_ln_mod_e4m3(c, W.x, mod + 3 * D, mod + 4 * D, 6LL * D, W.y8, W.sy, M, L, D, cfg->eps));
     else
-      WAN_TRY(launch_ln_mod(c, W.x, mod + 3 * D, mod + 4 * D, 6LL * D, W.y, f32, M, L, D, cfg->eps));
+      WAN_TRY(launch_ln_mod(c, W.x, mod + 3 * D, mod + 4 * D, 6LL * D, W.y, f32 ? OUT_F32 : OUT_BF16, M, L, D, cfg->eps));
     {
       EpiParams ep = epi_base(cfg->gelu_tanh ? EPI_GELU_TANH : EPI_GELU, M, Fh, L, bw.f1_b, f32);
       ep.out = W.h;
@@ -524,7 +547,7 @@ static int dit_forward_impl(const wan_dit_config* cfg, const wan_dit_weights* w,
   }
 
   // head: LN(x)(1+sc_h)+sh_h -> Linear D -> c_out*4 -> depatchify
-  WAN_TRY(launch_ln_mod(c, W.x, W.hm, W.hm + D, 2LL * D, W.y, f32, M, L, D, cfg->eps));
+  WAN_TRY(launch_ln_mod(c, W.x, W.hm, W.hm + D, 2LL * D, W.y, f32 ? OUT_F32 : OUT_BF16, M, L, D, cfg->eps));
   {
     EpiParams ep = epi_base(EPI_HEAD, M, cfg->c_out * 4, L, w->head_b, f32);
     ep.vout = v_out;
@@ -598,13 +621,14 @@ int wan_patchify(const float* latent, const void* w, const void* b, float* x, in
 
 int wan_adaln_modulate(const float* x, const float* shift, const float* scale, void* y, int B, int L, int D,
                        float eps, int dtype, wan_stream_t stream) {
-  WAN_TRY(check_dtype(dtype));
+  if (dtype != WAN_F16) WAN_TRY(check_dtype(dtype));
   if (!x || !y || B <= 0 || L <= 0 || D <= 0 || (!shift) != (!scale)) return WAN_ERR_INVALID_ARG;
   if (D % 4 || D > 8192 || !aligned16(x) || !aligned16(y) || (shift && (!aligned16(shift) || !aligned16(scale))))
     return WAN_ERR_UNSUPPORTED;
   LaunchCtx c;
   WAN_TRY(launch_ctx(stream, &c));
-  return launch_ln_mod(c, x, shift, scale, D, y, dtype == WAN_F32, B * L, L, D, eps);
+  return launch_ln_mod(c, x, shift, scale, D, y, dtype == WAN_F32 ? OUT_F32 : (dtype == WAN_F16 ? OUT_F16 : OUT_BF16),
+                       B * L, L, D, eps);
 }
 
 size_t wan_attn_workspace_size(int B, int L, int H, int d, int dtype) {
@@ -671,8 +695,14 @@ int wan_cross_attn(const void* q, const void* kt, const void* vt, const int* kt_
                    void* o, int B, int L, int Lt, int Li, int H, int d, int dtype, int qk_dtype, void* ws,
                    size_t ws_bytes, wan_stream_t stream) {
   (void)ws, (void)ws_bytes;
-  WAN_TRY(check_dtype(dtype));
-  WAN_TRY(check_qk_dtype(dtype, qk_dtype));
+  // dtype (v and o): WAN_F32 with fp32 q/k; WAN_BF16 with bf16 or fp16 q/k; WAN_F16 with fp16 q/k.
+  if (dtype == WAN_F16) {
+    if (qk_dtype != WAN_F16)
+      return (qk_dtype == WAN_BF16 || qk_dtype == WAN_F32) ? WAN_ERR_UNSUPPORTED : WAN_ERR_INVALID_ARG;
+  } else {
+    WAN_TRY(check_dtype(dtype));
+    WAN_TRY(check_qk_dtype(dtype, qk_dtype));
+  }
   const int f32 = dtype == WAN_F32;
   if (!q || !kt || !vt || !o || B <= 0 || L <= 0 || Lt <= 0 || Li < 0 || H <= 0 || d <= 0) return WAN_ERR_INVALID_ARG;
   if (Li > 0 && (!ki || !vi)) return WAN_ERR_INVALID_ARG;
@@ -682,22 +712,37 @@ int wan_cross_attn(const void* q, const void* kt, const void* vt, const int* kt_
   LaunchCtx c;
   WAN_TRY(launch_ctx(stream, &c));
   const int D = H * d;
-  for (int seg = 0; seg < (Li ? 2 : 1); ++seg) {
-    const int Lk = seg ? Li : Lt;
-    AttnArgs a;
-    memset(&a, 0, sizeof(a));
-    a.q = q; a.ldq = D; a.q_row_len = D;
-    a.k = seg ? ki : kt; a.ldk = D; a.k_row_len = D;
-    a.v = seg ? vi : vt; a.ldv = D; a.v_row_len = D;
-    a.o = o; a.ldo = D;
-    a.B = B; a.Lq = L; a.Lkv = Lk; a.H = H; a.head_dim = d;
-    a.accumulate = seg;
-    a.kv_lens = seg ? nullptr : kt_lens;
-    a.tag = "attn_cross";
-    a.qk_f16 = qk_dtype == WAN_F16;
-    WAN_TRY(attend(c, f32, a));
+  if (f32) {
+    for (int seg = 0; seg < (Li ? 2 : 1); ++seg) {
+      const int Lk = seg ? Li : Lt;
+      AttnArgs a;
+      memset(&a, 0, sizeof(a));
+      a.q = q; a.ldq = D; a.q_row_len = D;
+      a.k = seg ? ki : kt; a.ldk = D; a.k_row_len = D;
+      a.v = seg ? vi : vt; a.ldv = D; a.v_row_len = D;
+      a.o = o; a.ldo = D;
+      a.B = B; a.Lq = L; a.Lkv = Lk; a.H = H; a.head_dim = d;
+      a.accumulate = seg;
+      a.kv_lens = seg ? nullptr : kt_lens;
+      a.tag = "attn_cross";
+      WAN_TRY(attention_f32(c, a));
+    }
+    return WAN_OK;
   }
-  return WAN_OK;
+  CrossArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q; a.ldq = D; a.q_row_len = D;
+  a.kt = kt; a.vt = vt; a.ldkt = a.ldvt = D; a.kt_row_len = a.vt_row_len = D;
+  if (Li) {
+    a.ki = ki; a.vi = vi; a.ldki = a.ldvi = D; a.ki_row_len = a.vi_row_len = D;
+  }
+  a.o = o; a.ldo = D;
+  a.B = B; a.L = L; a.Lt = Lt; a.Li = Li; a.H = H; a.head_dim = d;
+  a.kt_lens = kt_lens;
+  a.qk_f16 = qk_dtype == WAN_F16;
+  a.pv_f16 = dtype == WAN_F16;
+  a.tag = "attn_cross";
+  return cross_attention_tc(c, a);
 }
 
 int wan_ffn(const void* y, const void* w1, const void* b1, const void* w2, const void* b2, const float* gate,
@@ -726,7 +771,7 @@ int wan_ffn(const void* y, const void* w1, const void* b1, const void* w2, const
 
 int wan_linear(const void* x, const void* w, const void* b, void* out, int M, int N, int K, int epilogue,
                const float* gate, int rows_per_gate, int dtype, int out_dtype, wan_stream_t stream) {
-  WAN_TRY(check_dtype(dtype));
+  if (dtype != WAN_F16) WAN_TRY(check_dtype(dtype));
   if (out_dtype != WAN_BF16 && out_dtype != WAN_F32 && out_dtype != WAN_F16) return WAN_ERR_INVALID_ARG;
   const int f32 = dtype == WAN_F32;
   if (!x || !w || !out || M <= 0 || N <= 0 || K <= 0) return WAN_ERR_INVALID_ARG;
@@ -756,7 +801,7 @@ int wan_linear(const void* x, const void* w, const void* b, void* out, int M, in
     ep.ldo = N;
     ep.out_type = out_dtype == WAN_F32 ? OUT_F32 : (out_dtype == WAN_F16 ? OUT_F16 : OUT_BF16);
   }
-  return proj(c, f32, x, K, K, w, K, K, M, N, K, 0, ep, "gemm_linear");
+  return proj(c, f32, x, K, K, w, K, K, M, N, K, 0, ep, "gemm_linear", dtype == WAN_F16);
 }
 
 static int out_type_of(int dtype) {

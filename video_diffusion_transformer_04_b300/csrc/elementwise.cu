@@ -89,6 +89,11 @@ __global__ void __launch_bounds__(128) ln_mod_kernel(const float* __restrict__ x
     if (c >= nv4) continue;
     if constexpr (sizeof(OutT) == 4) {
       reinterpret_cast<float4*>(y + (long long)row * D)[c] = make_float4(o[i][0], o[i][1], o[i][2], o[i][3]);
+    } else if constexpr (std::is_same<OutT, __half>::value) {
+      uint2 u;
+      u.x = pack_half2(o[i][0], o[i][1]);
+      u.y = pack_half2(o[i][2], o[i][3]);
+      reinterpret_cast<uint2*>(y + (long long)row * D)[c] = u;
     } else if constexpr (sizeof(OutT) == 2) {
       uint2 u;
       u.x = pack_bf16x2(o[i][0], o[i][1]);
@@ -112,12 +117,16 @@ static void ln_dispatch(const LaunchCtx& c, const float* x, const float* sh, con
 }
 
 int launch_ln_mod(const LaunchCtx& c, const float* x, const float* shift, const float* scale, long long mod_bstride,
-                  void* y, int out_f32, int rows, int L, int D, float eps) {
+                  void* y, int out_type, int rows, int L, int D, float eps) {
   if (rows <= 0) return WAN_OK;
   if (D % 4 != 0 || D > 8192) return WAN_ERR_UNSUPPORTED;
   count_launch("ln_modulate", c.stream, true);
-  if (out_f32) ln_dispatch<float>(c, x, shift, scale, mod_bstride, static_cast<float*>(y), nullptr, rows, L, D, eps);
-  else ln_dispatch<bf16>(c, x, shift, scale, mod_bstride, static_cast<bf16*>(y), nullptr, rows, L, D, eps);
+  if (out_type == OUT_F32)
+    ln_dispatch<float>(c, x, shift, scale, mod_bstride, static_cast<float*>(y), nullptr, rows, L, D, eps);
+  else if (out_type == OUT_F16)
+    ln_dispatch<__half>(c, x, shift, scale, mod_bstride, static_cast<__half*>(y), nullptr, rows, L, D, eps);
+  else
+    ln_dispatch<bf16>(c, x, shift, scale, mod_bstride, static_cast<bf16*>(y), nullptr, rows, L, D, eps);
   count_launch("ln_modulate", c.stream, false);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }

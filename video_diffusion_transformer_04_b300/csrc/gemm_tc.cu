@@ -1,9 +1,10 @@
 // bf16 GEMM on the 5th-generation tensor cores: C[M, N] = A[M, K] * B[N, K]^T with a
 // fused epilogue (epilogue.cuh).  Every projection of the DiT block (QKV, output,
 // cross-attention, FFN, patchify, head, text projection) runs through this kernel.
-// The FP8 instantiation (E4M3 A and B, kind::f8f6f4, 128 elements per 128-byte stage row)
-// multiplies the fp32 accumulator by the row scale of A and the column scale of B before
-// the same epilogue.
+// The operand type is a template parameter: bf16 or fp16 A and B (kind::f16; the
+// cross-attention projections run in fp16), or E4M3 (kind::f8f6f4, 128 elements per
+// 128-byte stage row), whose instantiation multiplies the fp32 accumulator by the row
+// scale of A and the column scale of B before the same epilogue.
 //
 // Design (one CTA per SM, persistent over output tiles of 128 x BN):
 //   warp 0      TMA producer: A and B tiles (128-byte swizzle) into a STAGES-deep ring
@@ -45,12 +46,16 @@ struct GemmCfg {
   static_assert(SMEM <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
-template <int BN, bool FP8>
+// Operand types of one GEMM instantiation (A and B always share one type).
+enum GemmAB : int { AB_BF16 = 0, AB_F16 = 1, AB_E4M3 = 2 };
+
+template <int BN, int AB>
 __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmR, const EpiParams ep, int M, int N, int K,
                         int kb_period, int* status) {
   using Cfg = GemmCfg<BN>;
+  constexpr bool FP8 = AB == AB_E4M3;
   constexpr int BK = FP8 ? 128 : 64;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -121,7 +126,8 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc = FP8 ? make_idesc_e4m3(Cfg::BM, BN) : make_idesc_bf16(Cfg::BM, BN);
+    constexpr uint32_t idesc = FP8 ? make_idesc_e4m3(Cfg::BM, BN)
+                                   : (AB == AB_F16 ? make_idesc_f16(Cfg::BM, BN) : make_idesc_bf16(Cfg::BM, BN));
     const uint32_t smem_lo0 = sdesc_sw128_lo(smem_u32(smem));
     int stage = 0;
     uint32_t phase = 0;
@@ -240,34 +246,33 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
   if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
-template <int BN, bool FP8>
+template <int BN, int AB>
 static int launch_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr,
                        const EpiParams& ep, int M, int N, int K, int kb_period, const char* tag) {
   using Cfg = GemmCfg<BN>;
   static std::atomic<unsigned long long> smem_set{0};
   {
-    const int st = set_smem_limit_once(reinterpret_cast<const void*>(gemm_bf16_tc_kernel<BN, FP8>), Cfg::SMEM, &smem_set);
+    const int st = set_smem_limit_once(reinterpret_cast<const void*>(gemm_bf16_tc_kernel<BN, AB>), Cfg::SMEM, &smem_set);
     if (st != WAN_OK) return st;
   }
   const int tiles = ((M + 127) / 128) * ((N + BN - 1) / BN);
   const int grid = tiles < c.num_sms ? tiles : c.num_sms;
   count_launch(tag, c.stream, true);
-  gemm_bf16_tc_kernel<BN, FP8><<<grid, Cfg::THREADS, Cfg::SMEM, c.stream>>>(ta, tb, tr, ep, M, N, K, kb_period,
-                                                                            c.dev_status);
+  gemm_bf16_tc_kernel<BN, AB><<<grid, Cfg::THREADS, Cfg::SMEM, c.stream>>>(ta, tb, tr, ep, M, N, K, kb_period,
+                                                                           c.dev_status);
   count_launch(tag, c.stream, false);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
 
-int gemm_bf16(const LaunchCtx& c, const bf16* A, long long lda, int a_cols, const bf16* B, long long ldb, int b_cols,
-              int M, int N, int K, int kb_period, const EpiParams& ep, const char* tag) {
+int gemm_bf16(const LaunchCtx& c, const void* A, long long lda, int a_cols, const void* B, long long ldb, int b_cols,
+              int M, int N, int K, int kb_period, const EpiParams& ep, const char* tag, bool ab_f16) {
   if (M <= 0 || N <= 0 || K <= 0) return WAN_OK;
   int bn = (N % 256 == 0) ? 256 : (N % 128 == 0 ? 128 : 64);
+  const CUtensorMapDataType dt = ab_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap ta, tb;
-  int st = make_tmap_2d(&ta, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a_cols, (uint64_t)M,
-                        (uint64_t)lda * 2, 64, 128);
+  int st = make_tmap_2d(&ta, A, dt, 2, (uint64_t)a_cols, (uint64_t)M, (uint64_t)lda * 2, 64, 128);
   if (st != WAN_OK) return st;
-  st = make_tmap_2d(&tb, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)b_cols, (uint64_t)N, (uint64_t)ldb * 2,
-                    64, (uint32_t)bn);
+  st = make_tmap_2d(&tb, B, dt, 2, (uint64_t)b_cols, (uint64_t)N, (uint64_t)ldb * 2, 64, (uint32_t)bn);
   if (st != WAN_OK) return st;
   CUtensorMap tr;
   memset(&tr, 0, sizeof(tr));
@@ -277,10 +282,17 @@ int gemm_bf16(const LaunchCtx& c, const bf16* A, long long lda, int a_cols, cons
                       (uint64_t)ep.ldr * 4, 32, 32);
     if (st != WAN_OK) return st;
   }
+  if (ab_f16) {
+    switch (bn) {
+      case 256: return launch_gemm<256, AB_F16>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
+      case 128: return launch_gemm<128, AB_F16>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
+      default: return launch_gemm<64, AB_F16>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
+    }
+  }
   switch (bn) {
-    case 256: return launch_gemm<256, false>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
-    case 128: return launch_gemm<128, false>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
-    default: return launch_gemm<64, false>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
+    case 256: return launch_gemm<256, AB_BF16>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
+    case 128: return launch_gemm<128, AB_BF16>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
+    default: return launch_gemm<64, AB_BF16>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
   }
 }
 
@@ -308,9 +320,9 @@ int gemm_e4m3(const LaunchCtx& c, const uint8_t* A, long long lda, int a_cols, c
     if (st != WAN_OK) return st;
   }
   switch (bn) {
-    case 256: return launch_gemm<256, true>(c, ta, tb, tr, ep, M, N, K, 0, tag);
-    case 128: return launch_gemm<128, true>(c, ta, tb, tr, ep, M, N, K, 0, tag);
-    default: return launch_gemm<64, true>(c, ta, tb, tr, ep, M, N, K, 0, tag);
+    case 256: return launch_gemm<256, AB_E4M3>(c, ta, tb, tr, ep, M, N, K, 0, tag);
+    case 128: return launch_gemm<128, AB_E4M3>(c, ta, tb, tr, ep, M, N, K, 0, tag);
+    default: return launch_gemm<64, AB_E4M3>(c, ta, tb, tr, ep, M, N, K, 0, tag);
   }
 }
 

@@ -23,11 +23,13 @@ int make_tmap_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int e
                  uint32_t box1);
 
 // ------------------------------------------------------------------ GEMMs
-// bf16 tcgen05 GEMM: C = A[M, K] * B[N, K]^T -> epilogue.  a_cols / b_cols: valid
-// columns of A / B (TMA zero-fills beyond); lda / ldb: row strides in elements.
-// kb_period > 0: the B k-block index wraps modulo kb_period (A = [hi | lo] split).
-int gemm_bf16(const LaunchCtx& c, const bf16* A, long long lda, int a_cols, const bf16* B, long long ldb,
-              int b_cols, int M, int N, int K, int kb_period, const EpiParams& ep, const char* tag);
+// 16-bit tcgen05 GEMM: C = A[M, K] * B[N, K]^T -> epilogue, A and B both bf16 (or both
+// fp16 when ab_f16).  a_cols / b_cols: valid columns of A / B (TMA zero-fills beyond);
+// lda / ldb: row strides in elements.  kb_period > 0: the B k-block index wraps modulo
+// kb_period (A = [hi | lo] split).
+int gemm_bf16(const LaunchCtx& c, const void* A, long long lda, int a_cols, const void* B, long long ldb,
+              int b_cols, int M, int N, int K, int kb_period, const EpiParams& ep, const char* tag,
+              bool ab_f16 = false);
 // FP8 (E4M3) tcgen05 GEMM: C = (A8 sa) (B8 sb)^T -> epilogue, with per-row scales sa [M]
 // of A and per-row scales sb [N] of B (per output channel) applied to the fp32
 // accumulator before the epilogue.  lda / ldb: row strides in bytes (multiples of 16).
@@ -61,6 +63,30 @@ struct AttnArgs {
   const char* tag; // profiler label of the launch
 };
 int attention_bf16(const LaunchCtx& c, const AttnArgs& a);
+
+// Decoupled cross-attention in one persistent launch (attn_cross.cu):
+//   o = softmax(q kt^T / sqrt(d)) vt [+ softmax(q ki^T / sqrt(d)) vi]
+// Rows are [B, len, ld*] with head h at columns *_col + h * d.  q and k are bf16 or fp16
+// (qk_f16); v and o are both bf16 or both fp16 (pv_f16, which needs qk_f16).
+struct CrossArgs {
+  const void* q;
+  long long ldq;
+  int q_row_len, q_col;
+  const void *kt, *vt;  // text keys / values [B, Lt, ld]
+  long long ldkt, ldvt;
+  int kt_row_len, vt_row_len, kt_col, vt_col;
+  const void *ki, *vi;  // image keys / values [B, Li, ld], or NULL when Li == 0
+  long long ldki, ldvi;
+  int ki_row_len, vi_row_len, ki_col, vi_col;
+  void* o;
+  long long ldo;
+  int o_col;
+  int B, L, Lt, Li, H, head_dim;
+  const int* kt_lens;  // device [B]: valid text keys per batch entry (clamped to [1, Lt]), or NULL
+  int qk_f16, pv_f16;
+  const char* tag;
+};
+int cross_attention_tc(const LaunchCtx& c, const CrossArgs& a);
 int attention_f32(const LaunchCtx& c, const AttnArgs& a);
 
 // ------------------------------------------------------------------ 8-bit operands and attention
@@ -111,8 +137,9 @@ int launch_ln_mod_e4m3(const LaunchCtx& c, const float* x, const float* shift, c
                        long long mod_bstride, uint8_t* y8, float* sy, int rows, int L, int D, float eps);
 
 // ------------------------------------------------------------------ elementwise / small kernels
+// y = LN(x)(1 + scale) + shift per row, stored as out_type (OutType: bf16, fp16 or fp32).
 int launch_ln_mod(const LaunchCtx& c, const float* x, const float* shift, const float* scale, long long mod_bstride,
-                  void* y, int out_f32, int rows, int L, int D, float eps);
+                  void* y, int out_type, int rows, int L, int D, float eps);
 int launch_cfg_euler(const LaunchCtx& c, float* x, const void* vc, const void* vu, long long n, float s, float dt,
                      const float* t_pair, int v_f32);
 int launch_patch_gather(const LaunchCtx& c, const float* latent, long long latent_bstride, void* A, int out_f32,

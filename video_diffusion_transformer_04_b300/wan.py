@@ -340,9 +340,13 @@ class DiT:
             text_len=shape.text_len, img_len=shape.img_len, freq_dim=shape.freq_dim, theta=shape.theta,
             eps=shape.eps, qk_norm=int(getattr(shape, "qk_norm", False)),
             gelu_tanh=int(getattr(shape, "gelu_tanh", False)), fp8=int(getattr(shape, "fp8", 0)))
-        up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=self.tdtype)
+        up = lambda a, dt=self.tdtype: torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=dt)
         self.tensors = {k: up(v) for k, v in weights.items() if k != "blocks"}
-        self.block_tensors = [{k: up(v) for k, v in blk.items()} for blk in weights["blocks"]]
+        # In the 16-bit configuration the cross-attention query and output projections
+        # are stored in fp16 (libwan runs that sub-layer in fp16, include/wan.h).
+        f16 = {"cq_w", "co_w"} if self.tdtype == torch.bfloat16 else set()
+        self.block_tensors = [{k: up(v, torch.float16 if k in f16 else self.tdtype) for k, v in blk.items()}
+                              for blk in weights["blocks"]]
         if self.cfg.fp8 & 2:  # E4M3 codes + per-output-channel scales of the QKV and FFN-up weights
             for bt in self.block_tensors:
                 for n in ("qkv_w", "f1_w"):
