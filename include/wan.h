@@ -133,6 +133,27 @@ int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, const 
                     int L, int H, int d, int Fg, int Hg, int Wg, float theta, int apply_rope, int dtype,
                     int qk_dtype, void* ws, size_t ws_bytes, wan_stream_t stream);
 
+/* ------------------------------------------------------------------ QKV projection + 3D RoPE
+ * [Code] q, k, v = projections of the modulated input, then rope_apply(q | k, grid_sizes,
+ * freqs): the self-attention's QKV projection with the rotation fused into its epilogue
+ * (the same kernel as inside wan_dit_forward).
+ *   qkv[b, l, :] = [q | k | v] = y[b, l, :] w^T + b, then q and k of every head rotated
+ *   as described for wan_attn_rope3d (grid (Fg, Hg, Wg), Fg*Hg*Wg == L, base theta).
+ * y: [B, L, D] (dtype: WAN_BF16 or WAN_F32), D = H*d; w: [3D, D]; b: [3D] or NULL (dtype).
+ * qkv: [B, L, 3D]; with WAN_BF16 the q and k columns [0, 2D) hold fp16 values and the v
+ * columns bf16 (the storage the attention kernels take); with WAN_F32 all fp32.
+ * ws: >= wan_qkv_rope_workspace_size(d) bytes, 16-byte aligned (the pair frequencies).
+ * wan_qkv_rope_e4m3: the FP8 form of the 8-bit variant: y8 [B*L, D] E4M3 codes with row
+ * scales sy [B*L], w8 [3D, D] codes with row scales sw [3D] (as wan_quant_rows_e4m3
+ * writes them), b bf16; output as for WAN_BF16.  Needs D % 32 == 0 (and d % 32 == 0
+ * with 16-bit output). */
+size_t wan_qkv_rope_workspace_size(int d);
+int wan_qkv_rope(const void* y, const void* w, const void* b, void* qkv, int B, int L, int H, int d, int Fg,
+                 int Hg, int Wg, float theta, int dtype, void* ws, size_t ws_bytes, wan_stream_t stream);
+int wan_qkv_rope_e4m3(const void* y8, const float* sy, const void* w8, const float* sw, const void* b,
+                      void* qkv, int B, int L, int H, int d, int Fg, int Hg, int Wg, float theta, void* ws,
+                      size_t ws_bytes, wan_stream_t stream);
+
 /* ------------------------------------------------------------------ cross-attention
  * [Method] text conditioning by cross-attention; [I2V] decoupled cross-attention to the
  * CLIP image context: o = softmax(q kt^T/sqrt(d)) vt + softmax(q ki^T/sqrt(d)) vi

@@ -80,6 +80,33 @@ def test_host_validation_rejects_bad_arguments(wanlib):
     assert h(None, None, None, None, None, None, None, 1, 8, 8, 0, 1, 64, 0, 2, None, 0, None) == -1  # NULL q
 
 
+def test_host_validation_of_the_fp16_and_qkv_rope_entry_points(wanlib):
+    P, I, F, SZ = C.c_void_p, C.c_int, C.c_float, C.c_size_t
+    A = 1 << 12
+    h = wanlib.wan_cross_attn
+    h.argtypes = [C.c_void_p] * 7 + [C.c_int] * 8 + [C.c_void_p, C.c_size_t, C.c_void_p]
+    # fp16 v/o (the forward's cross-attention) need fp16 q/k
+    assert h(A, A, A, None, None, None, A, 1, 8, 8, 0, 1, 64, 2, 0, None, 0, None) == -2
+    assert h(None, A, A, None, None, None, A, 1, 8, 8, 0, 1, 64, 2, 2, None, 0, None) == -1
+    g = wanlib.wan_linear
+    g.argtypes = [C.c_void_p] * 4 + [C.c_int] * 4 + [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p]
+    assert g(None, A, None, A, 8, 64, 64, 0, None, 0, 2, 2, None) == -1   # fp16 operands: NULL x
+    assert g(A, A, None, A, 8, 48, 64, 0, None, 0, 2, 2, None) == -2      # N % 32
+    r = wanlib.wan_qkv_rope
+    r.argtypes = [P] * 4 + [I] * 7 + [F, I, P, SZ, P]
+    assert wanlib.wan_qkv_rope_workspace_size(128) >= 64 * 4
+    ok = [A, A, A, A, 1, 60, 2, 128, 3, 4, 5, 10000.0, 0]
+    assert r(None, *ok[1:], A, 1024, None) == -1                      # NULL y
+    assert r(*ok[:8], 3, 4, 6, 10000.0, 0, A, 1024, None) == -1       # grid does not cover L
+    assert r(*ok, None, 0, None) == -5                                # no workspace
+    assert r(*ok[:12], 7, A, 1024, None) == -1                        # unknown dtype
+    r8 = wanlib.wan_qkv_rope_e4m3
+    r8.argtypes = [P] * 6 + [I] * 7 + [F, P, SZ, P]
+    args8 = [A, A, A, A, A, A, 1, 60, 2, 128, 3, 4, 5, 10000.0]
+    assert r8(A, None, *args8[2:], A, 1024, None) == -1               # missing row scales
+    assert r8(*args8, A, 8, None) == -5                               # workspace too small
+
+
 def test_dit_workspace_size_arithmetic():
     import synth
     from video_diffusion_transformer_04_b300 import wan

@@ -12,17 +12,14 @@
   with p_j the exact probabilities relative to the row max.
 * FP8 GEMM, fed the oracle's codes: every product of two codes is exact, the sum is fp32,
   so the bf16 tolerances of the other GEMMs apply (fp32 tolerance for the residual form).
-* The forward with the variant on, against the oracle's 8-bit forward.  Each side takes its
-  quantisation decisions on its own activations (bf16 on the GPU, fp64 in the oracle), so
-  where a value lies within bf16 rounding of an E4M3 rounding boundary the two codes
-  differ by one step: with a relative spacing of 2^-3 against bf16's 2^-8 that is a few
-  percent of the codes, each off by up to a full step where the oracle is off by at most
-  half of one.  Their effect is of the order of half the quantisation error itself, so the
-  tolerances are the bf16 ones widened by half of the oracle's own 8-bit-vs-exact
-  difference (max |.|/RMS and mean relative alike); the kernel's probability rounding,
-  unmodelled, sits inside the same allowance.  At the full-size blocks, where quantisation
-  moves the result well beyond bf16 rounding, the GPU result must also lie closer to the
-  8-bit oracle than to the exact one: it computes the 8-bit method, not the bf16 one.
+* The forward with the variant on, against the oracle's 8-bit forward, within the plain
+  bf16 tolerances: the tiny configuration and the full 1.3B block.  At the full 1.3B
+  block, where quantisation moves the result well beyond bf16 rounding, the GPU result
+  must also lie closer to the 8-bit oracle than to the exact one: it computes the 8-bit
+  method, not the bf16 one.  (At the tiny size the quantisation error is below the bf16
+  rounding, so that comparison says nothing there.)  The 14B I2V block, where each side's
+  own quantisation decisions on its own activations differ in a few percent of the codes,
+  is checked in tests/test_gpu_block_fp8.py with the oracle fed the GPU's codes.
 """
 import os
 
@@ -32,8 +29,7 @@ import torch
 
 import synth
 from oracle import wan_oracle as O
-from tests.parity import (BF16_MAX_ABS_OVER_RMS, BF16_MEAN_REL, _log, assert_bf16_close, assert_f32_close,
-                          bf16_errors, to_dev, to_np, tokens_of)
+from tests.parity import _log, assert_bf16_close, assert_f32_close, to_dev, to_np, tokens_of
 
 pytestmark = pytest.mark.gpu
 BF, F16, F32, U8 = torch.bfloat16, torch.float16, torch.float32, torch.uint8
@@ -57,17 +53,6 @@ def _u8(t):
 def _rel_rms(a, b):
     a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
     return float(np.sqrt(np.mean((a - b) ** 2) / np.mean(b ** 2)))
-
-
-def assert_fp8_close(g, o8, ex, what):
-    """bf16 tolerances widened by half the 8-bit quantisation effect (module docstring)."""
-    mx_q, mr_q = bf16_errors(o8, ex)
-    mx, mr = bf16_errors(g, o8)
-    tol_mx, tol_mr = BF16_MAX_ABS_OVER_RMS + 0.5 * mx_q, BF16_MEAN_REL + 0.5 * mr_q
-    _log(what=what, kind="fp8_tol", max_abs_over_rms=mx, mean_rel=mr, tol_max=tol_mx, tol_mean=tol_mr,
-         ok=bool(mx <= tol_mx and mr <= tol_mr))
-    assert mx <= tol_mx and mr <= tol_mr, \
-        f"{what}: max|err|/rms = {mx:.3e} (<= {tol_mx:.3e}), mean rel = {mr:.3e} (<= {tol_mr:.3e})"
 
 
 # ---------------------------------------------------------------- quantisers
@@ -268,10 +253,10 @@ def test_tiny_forward_fp8_variant(wan, bits):
     ex = O.dit_forward(lat, t, ctx_o, None, w, s.replace(fp8=0))
     _log(what=f"tiny fp8={bits}", kind="fp8_forward", gpu_vs_oracle8=_rel_rms(g, o8), oracle8_vs_exact=_rel_rms(o8, ex),
          ok=True)
-    assert_fp8_close(g, o8, ex, f"tiny forward fp8={bits}")
+    assert_bf16_close(g, o8, f"tiny forward fp8={bits}")
 
 
-@pytest.mark.parametrize("name", ["wan1.3b-block", "wan14b-i2v-block"])
+@pytest.mark.parametrize("name", ["wan1.3b-block"])
 def test_single_block_fp8_variant(wan, name):
     path8 = os.path.join(GOLDEN, f"{name}-fp8.npz")
     path = os.path.join(GOLDEN, f"{name}.npz")
@@ -293,6 +278,6 @@ def test_single_block_fp8_variant(wan, name):
     e_exact = _rel_rms(head, gx["head"])
     _log(what=f"{name} fp8", kind="fp8_forward", gpu_vs_oracle8=e_gpu, oracle8_vs_exact=e_q, gpu_vs_exact=e_exact,
          ok=bool(e_gpu <= e_q and e_gpu < 0.5 * e_exact))
-    assert_fp8_close(head, g8["head"], gx["head"], f"{name} fp8 head rows")
+    assert_bf16_close(head, g8["head"], f"{name} fp8 head rows")
     assert e_gpu <= e_q and e_gpu < 0.5 * e_exact, \
         f"|gpu - oracle8| {e_gpu:.3e}, |oracle8 - exact| {e_q:.3e}, |gpu - exact| {e_exact:.3e}"

@@ -686,6 +686,59 @@ int wan_attn_rope3d(const void* q, const void* k, const void* v, void* o, const 
   return attend(c, f32, a);
 }
 
+size_t wan_qkv_rope_workspace_size(int d) {
+  if (d <= 0) return 0;
+  return (size_t)round_up((long long)d / 2 * 4, 1024);
+}
+
+// The QKV projection of the forward with its fused epilogue: bias, 3D RoPE on q and k,
+// q and k stored in fp16 (16-bit path) next to v in the call's type.
+static int qkv_rope_common(const void* y, const float* sy, const void* w, const float* sw, const void* b, void* qkv,
+                           int B, int L, int H, int d, int Fg, int Hg, int Wg, float theta, int dtype, bool e4m3,
+                           void* ws, size_t ws_bytes, cudaStream_t stream) {
+  const int f32 = dtype == WAN_F32;
+  if (!y || !w || !qkv || B <= 0 || L <= 0 || H <= 0 || d <= 0 || d % 2) return WAN_ERR_INVALID_ARG;
+  if (Fg <= 0 || Hg <= 0 || Wg <= 0 || (long long)Fg * Hg * Wg != L) return WAN_ERR_INVALID_ARG;
+  if (e4m3 && (!sy || !sw)) return WAN_ERR_INVALID_ARG;
+  const int D = H * d;
+  if (D % 32 || (!f32 && d % 32) || !aligned16(y) || !aligned16(w) || !aligned16(qkv) || (b && !aligned16(b)) ||
+      (sw && !aligned16(sw)))
+    return WAN_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < wan_qkv_rope_workspace_size(d) || !aligned16(ws)) return WAN_ERR_WORKSPACE;
+  LaunchCtx c;
+  WAN_TRY(launch_ctx(stream, &c));
+  float* tab = static_cast<float*>(ws);
+  WAN_TRY(launch_rope_table(c, tab, d, theta));
+  const int M = B * L;
+  EpiParams ep = epi_base(EPI_QKV, M, 3 * D, L, b, f32);
+  ep.out = qkv;
+  ep.ldo = 3LL * D;
+  ep.out_type = f32 ? OUT_F32 : OUT_BF16;
+  ep.n_rot = 2 * D;
+  ep.n_f16 = f32 ? 0 : 2 * D;
+  ep.head_dim = d;
+  ep.rope = rope_geom(tab, Fg, Hg, Wg, d);
+  if (e4m3)
+    return gemm_e4m3(c, static_cast<const uint8_t*>(y), D, D, sy, static_cast<const uint8_t*>(w), D, D, sw, M, 3 * D,
+                     D, ep, "gemm_qkv_rope_e4m3");
+  return proj(c, f32, y, D, D, w, D, D, M, 3 * D, D, 0, ep, "gemm_qkv_rope");
+}
+
+int wan_qkv_rope(const void* y, const void* w, const void* b, void* qkv, int B, int L, int H, int d, int Fg, int Hg,
+                 int Wg, float theta, int dtype, void* ws, size_t ws_bytes, wan_stream_t stream) {
+  WAN_TRY(check_dtype(dtype));
+  return qkv_rope_common(y, nullptr, w, nullptr, b, qkv, B, L, H, d, Fg, Hg, Wg, theta, dtype, false, ws, ws_bytes,
+                         stream);
+}
+
+int wan_qkv_rope_e4m3(const void* y8, const float* sy, const void* w8, const float* sw, const void* b, void* qkv,
+                      int B, int L, int H, int d, int Fg, int Hg, int Wg, float theta, void* ws, size_t ws_bytes,
+                      wan_stream_t stream) {
+  if ((long long)H * d % 16) return WAN_ERR_UNSUPPORTED;
+  return qkv_rope_common(y8, sy, w8, sw, b, qkv, B, L, H, d, Fg, Hg, Wg, theta, WAN_BF16, true, ws, ws_bytes,
+                         stream);
+}
+
 size_t wan_cross_attn_workspace_size(int B, int Lt, int Li, int H, int d, int dtype) {
   (void)B, (void)Lt, (void)Li, (void)H, (void)d, (void)dtype;
   return 0;  // the kernels read q, k and v in place

@@ -71,6 +71,9 @@ _SIGS = {
     "wan_adaln_modulate": (I, [P, P, P, P, I, I, I, F, I, P]),
     "wan_attn_workspace_size": (SZ, [I, I, I, I, I]),
     "wan_attn_rope3d": (I, [P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, P, SZ, P]),
+    "wan_qkv_rope_workspace_size": (SZ, [I]),
+    "wan_qkv_rope": (I, [P, P, P, P, I, I, I, I, I, I, I, F, I, P, SZ, P]),
+    "wan_qkv_rope_e4m3": (I, [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, SZ, P]),
     "wan_cross_attn_workspace_size": (SZ, [I, I, I, I, I, I]),
     "wan_cross_attn": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, SZ, P]),
     "wan_ffn": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, P]),
@@ -182,6 +185,26 @@ def wan_attn_rope3d(q, k, v, o, grid, theta=10000.0, apply_rope=True, ws=None, k
     _check(lib.wan_attn_rope3d(_p(q), _p(k), _p(v), _p(o), _p(kv_lens), B, L, H, d, grid[0], grid[1], grid[2], theta,
                                1 if apply_rope else 0, dtype_code(v.dtype), dtype_code(q.dtype), _p(ws),
                                _nbytes(ws), _stream(stream)), "wan_attn_rope3d")
+
+
+def wan_qkv_rope(y, w, b, qkv, heads, grid, theta=10000.0, ws=None, stream=None):
+    """y [B, L, D] -> qkv [B, L, 3D] (q, k rotated; fp16 q|k next to bf16 v for bf16 y)."""
+    B, L, D = y.shape
+    d = D // heads
+    if ws is None:
+        ws = torch.empty(lib.wan_qkv_rope_workspace_size(d), dtype=torch.uint8, device=y.device)
+    _check(lib.wan_qkv_rope(_p(y), _p(w), _p(b), _p(qkv), B, L, heads, d, grid[0], grid[1], grid[2], theta,
+                            dtype_code(y.dtype), _p(ws), _nbytes(ws), _stream(stream)), "wan_qkv_rope")
+
+
+def wan_qkv_rope_e4m3(y8, sy, w8, sw, b, qkv, heads, grid, theta=10000.0, ws=None, stream=None):
+    """E4M3 rows y8 [B, L, D] (scales sy [B*L]) -> qkv [B, L, 3D] as wan_qkv_rope writes it."""
+    B, L, D = y8.shape
+    d = D // heads
+    if ws is None:
+        ws = torch.empty(lib.wan_qkv_rope_workspace_size(d), dtype=torch.uint8, device=y8.device)
+    _check(lib.wan_qkv_rope_e4m3(_p(y8), _p(sy), _p(w8), _p(sw), _p(b), _p(qkv), B, L, heads, d, grid[0], grid[1],
+                                 grid[2], theta, _p(ws), _nbytes(ws), _stream(stream)), "wan_qkv_rope_e4m3")
 
 
 def wan_cross_attn_workspace_size(B, Lt, Li, H, d, dtype):
