@@ -2,13 +2,17 @@
 """Benchmark of the Wan DiT guided denoising step on B300 (libwan, sm_103a).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload wan1.3b-30blk-guided-step | wan1.3b-block | wan14b-i2v-block]
+                    [--workload wan1.3b-30blk-guided-step | wan1.3b-block | wan14b-i2v-block |
+                                wan1.3b-20step-sampler]
 
 One step = one pass of the whole hot path over the 30-block 1.3B-shaped DiT at 480p
 (21x60x104 latent -> 32760 tokens), batch 2 (cond + uncond): text projection, time
 embedding, patchify, 30 blocks (AdaLN, QKV + 3D RoPE, self-attention, cross-attention,
 GELU FFN, gated residuals), head + depatchify, fused CFG + Euler update.  Synthetic
 seeded inputs, random-init weights ~N(0, 0.02).  Rank 0 prints one JSON line.
+
+The 20-step sampler workload times one whole generation per bench step (text projection,
+every block's cross-attention keys/values once, 20 guided steps on the uniform schedule).
 
 --impl reference times the CPU fp64 oracle (the method's plain definition) on the
 host cores, on a bounded sample of the same workload, and extrapolates to one step.
@@ -47,7 +51,9 @@ def peaks():
 
 
 def step_macs(s) -> dict:
-    """Algorithmic multiply-accumulates of one guided step, by role."""
+    """Algorithmic multiply-accumulates of one guided step, by role (for the sampler: one
+    whole generation, whose text projection and cross-attention keys/values are computed
+    once and reused by every step)."""
     B, L, D, F, Lt, Li = s.batch, s.tokens, s.dim, s.ffn, s.text_len, s.img_len
     m = {
         "text": B * Lt * (s.text_dim * D + D * D) if s.text_dim else 0,
@@ -62,6 +68,10 @@ def step_macs(s) -> dict:
         "ffn": s.blocks * B * L * 2 * D * F,
         "head": B * L * D * s.c_out * 4,
     }
+    if s.steps > 1:
+        for k in m:
+            if k not in ("text", "cross_kv"):
+                m[k] *= s.steps
     return m
 
 
@@ -128,7 +138,18 @@ def blas_threads() -> int:
     return len(os.sched_getaffinity(0))
 
 
-def oracle_step_estimate(s, seed=0, rows_small=1, rows_large=2049):
+def cpu_model() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
+def oracle_step_estimate(s, seed=0, rows_small=1, rows_large=513):
     """Time the fp64 oracle on a bounded sample of one block and extrapolate to a step.
 
     Sample: one 1.3B-shaped block on batch entry 0, run twice: with `rows_small` query
@@ -156,12 +177,43 @@ def oracle_step_estimate(s, seed=0, rows_small=1, rows_large=2049):
     per_row = max((times[rows_large] - times[rows_small]) / (rows_large - rows_small), 1e-12)
     fixed = max(times[rows_small] - rows_small * per_row, 0.0)
     block = fixed + one.tokens * per_row
-    step = block * s.batch * s.blocks
+    step = block * s.batch * s.blocks * max(s.steps, 1)
     threads = blas_threads()
     sample = (f"one {one.dim}-wide block, batch entry 0: full LN+QKV over {one.tokens} tokens plus "
               f"{rows_small} and {rows_large} query rows end to end ({sum(times.values()):.1f} s of CPU); "
-              f"extrapolated x{s.batch} batch x{s.blocks} blocks")
+              f"extrapolated x{s.batch} batch x{s.blocks} blocks" + (f" x{s.steps} steps" if s.steps > 1 else ""))
     return step, threads, sample, sum(times.values())
+
+
+def oracle_baseline(s, repeats=3):
+    """The oracle's rate on this host: `repeats` all-core samples (mean and spread) and one
+    single-threaded sample, the same sampling method as the reference arm."""
+    units = s.batch * s.tokens * max(s.steps, 1)
+    runs, sample, threads, spent = [], "", 1, 0.0
+    for _ in range(repeats):
+        step_s, threads, sample, cpu_s = oracle_step_estimate(s)
+        runs.append(units / step_s)
+        spent += cpu_s
+    # Single-threaded: a child process whose BLAS starts with one thread.
+    single = None
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, bench, synth; s = synth.WORKLOADS[%r].replace(batch=%d); "
+            "r = bench.oracle_step_estimate(s); print(json.dumps([r[0], r[1], r[3]]))" % (s.name, s.batch))
+    try:
+        out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                             timeout=600)
+        step_s, th, cpu_s = json.loads(out.stdout.strip().splitlines()[-1])
+        if th == 1:
+            single = units / step_s
+        spent += cpu_s
+    except (subprocess.SubprocessError, ValueError, IndexError):
+        pass
+    return {"value": round(statistics.mean(runs), 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": sample, "repeats": [round(r, 3) for r in runs],
+            "spread": round((max(runs) - min(runs)) / statistics.mean(runs), 4),
+            "single_thread_value": None if single is None else round(single, 3),
+            "cpu_model": cpu_model(), "nproc": os.cpu_count(), "affinity": len(os.sched_getaffinity(0)),
+            "cpu_seconds": round(spent, 1)}
 
 
 # ---------------------------------------------------------------- multi-rank bookkeeping
@@ -214,10 +266,16 @@ def run_ours(a, s):
     t_pair = t_pair_h.to(dev)
     v_ws = torch.empty(2, s.c_out, s.frames, s.height, s.width, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    sampler = s.steps > 1
+    noise = x.clone() if sampler else None
 
     def step():
         ctx = m.text_embed(text) if s.text_dim else ctx_fixed
-        m.guided_step(x, t_pair, s.guide_scale, ctx, ctx_img, v_ws=v_ws)
+        if sampler:  # one whole generation from the same noise
+            x.copy_(noise)
+            m.sample(x, s.steps, s.guide_scale, ctx, ctx_img)
+        else:
+            m.guided_step(x, t_pair, s.guide_scale, ctx, ctx_img, v_ws=v_ws)
 
     for _ in range(a.warmup):
         step()
@@ -234,18 +292,30 @@ def run_ours(a, s):
     clocks.start()
     time.sleep(0.3)
     launches0 = wan.wan_launch_count()
-    wan.wan_profile_begin(1 << 17)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(a.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    prof = wan.wan_profile_end()
     launches = wan.wan_launch_count() - launches0
     clk = clocks.stop()
     wan.wan_sync_status()
     ms = max_over_ranks(e0.elapsed_time(e1), dev)
+
+    # ---- the per-kernel split: a separate pass with CUDA events around every launch
+    # (not the timed region above), sampled clocks alongside.
+    prof_steps = 1 if sampler else a.steps
+    pclocks = Clocks(gpu_id)
+    pclocks.start()
+    time.sleep(0.3)
+    wan.wan_profile_begin(1 << 17)
+    for _ in range(prof_steps):
+        step()
+    torch.cuda.synchronize(dev)
+    prof = wan.wan_profile_end()
+    pclk = pclocks.stop()
+    wan.wan_sync_status()
 
     # ---- end to end through the public API with host buffers (copies inside the timed region)
     x_out_h = torch.empty_like(lat_h).pin_memory()
@@ -253,7 +323,7 @@ def run_ours(a, s):
     d2h = x_out_h.numel() * 4
 
     def step_host():
-        x.copy_(lat_h, non_blocking=True)
+        (noise if sampler else x).copy_(lat_h, non_blocking=True)
         t_pair.copy_(t_pair_h, non_blocking=True)
         if s.text_dim:
             text.copy_(text_h, non_blocking=True)
@@ -272,7 +342,9 @@ def run_ours(a, s):
     torch.cuda.synchronize(dev)
     ms_e2e = max_over_ranks(f0.elapsed_time(f1), dev)
 
-    tokens_per_step = s.batch * s.tokens
+    tokens_per_step = s.batch * s.tokens * max(s.steps, 1)
+    weight_gb = sum(t.numel() * t.element_size() for bt in m.block_tensors for t in bt.values()) / 1e9
+    ws_gb = m.ws.numel() / 1e9
     value = aggregate_rate(tokens_per_step, a.steps, world, ms)
     macs = step_macs(s)
     flop_step = 2 * sum(macs.values())
@@ -280,25 +352,33 @@ def run_ours(a, s):
     tflops = flop_step * a.steps / (ms / 1e3) / 1e12
 
     total_prof = sum(v[0] for v in prof.values()) or 1.0
-    kernels = {k: {"ms_per_step": round(v[0] / a.steps, 3), "launches_per_step": v[1] / a.steps,
+    kernels = {k: {"ms_per_step": round(v[0] / prof_steps, 3), "launches_per_step": v[1] / prof_steps,
                    "share": round(v[0] / total_prof, 4)} for k, v in sorted(prof.items(), key=lambda kv: -kv[1][0])}
     fp8_attn = bool(s.fp8 & 1)
     dom = "attn_self_e4m3" if fp8_attn else "attn_self"
     roof = None
     if dom in prof:
-        per_launch_flop = 2 * macs["self_attn"] / (s.blocks)   # one launch = one block, whole batch
+        per_launch_flop = 2 * macs["self_attn"] / (s.blocks * max(s.steps, 1))  # one launch = one block, whole batch
         avg_ms = prof[dom][0] / prof[dom][1]
         achieved = per_launch_flop / (avg_ms / 1e3) / 1e12
+        mhz = pclk.get("sm_mhz")
+        clock_scaled = achieved / (mhz / pk["sm_max_mhz"]) if mhz and pk.get("sm_max_mhz") else None
         # E4M3 tensor peak: the measured bf16 figure times the nominal dense ratio 4.5 / 2.25
         peak = pk["bf16_tflops_sustained"] * (2.0 if fp8_attn else 1.0)
         kind = "e4m3 sustained = 2 x measured bf16 sustained (nominal ratio)" if fp8_attn else "bf16 sustained"
+        burst = pk["bf16_tflops"] * (2.0 if fp8_attn else 1.0)
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "peak_kind": f"{kind} ({pk_kind})",
+                "frac_of_burst": round(achieved / burst, 4),
+                "achieved_at_max_clock": None if clock_scaled is None else round(clock_scaled, 1),
+                "frac_of_burst_at_max_clock": None if clock_scaled is None else round(clock_scaled / burst, 4),
+                "profiled_sm_mhz": mhz,
                 "flop_per_launch": per_launch_flop, "avg_launch_ms": round(avg_ms, 4),
                 "traffic": traffic_record(dom)}
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "per_guided_latent_tokens_per_s": round(value / s.batch, 1),
         "warmup": a.warmup, "ms_per_step": round(ms / a.steps, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if not s.fp8 else "bf16 + e4m3", "data": "synthetic (seeded N(0,1) latent and text, N(0,0.02) weights)",
         "config": {"workload": s.name, "blocks": s.blocks, "batch": s.batch,
@@ -307,7 +387,10 @@ def run_ours(a, s):
                    "img_len": s.img_len, "guide_scale": s.guide_scale,
                    "variant": {"qk_norm": s.qk_norm, "gelu_tanh": s.gelu_tanh, "fp8": s.fp8},
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2: 2.8 GB of weights and ~3 GB of activations stream every step"},
+                   "units": ("latent tokens of both CFG branches (batch 2) per DiT step"
+                             + (f", {s.steps} steps per generation" if sampler else "")),
+                   "l2": (f"inputs larger than L2 (126 MB): {weight_gb:.2f} GB of weights and {ws_gb:.1f} GB of "
+                          "workspace stream through every step, so no flush is needed between steps")},
         "tflops": round(tflops, 1), "bf16_peak_frac": round(tflops / pk["bf16_tflops"], 4),
         "bf16_sustained_frac": round(tflops / pk["bf16_tflops_sustained"], 4),
         "flop_per_step": flop_step,
@@ -320,10 +403,7 @@ def run_ours(a, s):
     }
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         print(json.dumps({"partial": out}), file=sys.stderr, flush=True)
-        step_s, threads, sample, spent = oracle_step_estimate(s)
-        out["cpu_baseline"] = {"value": round(tokens_per_step / step_s, 3), "unit": UNIT, "cores": threads,
-                               "kind": "oracle", "sample": sample, "cpu_seconds": round(spent, 1),
-                               "step_seconds_extrapolated": round(step_s, 1)}
+        out["cpu_baseline"] = oracle_baseline(s)
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:
@@ -362,18 +442,22 @@ def run_reference(a, s):
     est = []
     threads, sample = 1, ""
     for i in range(a.warmup + a.steps):
-        step_s, threads, sample, _ = oracle_step_estimate(s, rows_small=1, rows_large=513)
+        step_s, threads, sample, _ = oracle_step_estimate(s)
         if i >= a.warmup:
             est.append(step_s)
     step_s = statistics.mean(est)
-    value = s.batch * s.tokens / step_s
+    units = s.batch * s.tokens * max(s.steps, 1)
+    value = units / step_s
+    rates = [units / e for e in est]
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1,
            "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(step_s * 1e3, 1), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": s.name, "tokens": s.tokens, "blocks": s.blocks,
                       "batch": s.batch},
            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
-                            "sample": sample},
+                            "sample": sample, "repeats": [round(r, 3) for r in rates],
+                            "spread": round((max(rates) - min(rates)) / statistics.mean(rates), 4),
+                            "cpu_model": cpu_model(), "nproc": os.cpu_count()},
            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
@@ -385,7 +469,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="wan1.3b-30blk-guided-step",
-                    choices=["wan1.3b-30blk-guided-step", "wan1.3b-block", "wan14b-i2v-block"])
+                    choices=["wan1.3b-30blk-guided-step", "wan1.3b-block", "wan14b-i2v-block",
+                             "wan1.3b-20step-sampler"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--qk-norm", action="store_true", help="variant: RMSNorm on q and k before RoPE")
     ap.add_argument("--gelu-tanh", action="store_true", help="variant: tanh-form GELU in the FFN")

@@ -289,6 +289,37 @@ def test_attn_full_size_sampled_rows(wan):
     assert_bf16_close(to_np(o[0, rows]), ref, "attn full-size")
 
 
+@pytest.mark.parametrize("qkt", ["f16", "bf16"])
+def test_attn_full_size_peaked_late_rising_max(wan, qkt):
+    # The 1.3B self-attention shape with sharp softmaxes: logits of std 5 (q ~ N(0, 25),
+    # k ~ N(0, 1)), and keys whose norm grows over the last eighth of the sequence, so
+    # each row's maximum keeps rising late and the lazy rescale runs deep into the key
+    # loop.  Checked on sampled query rows against every key.
+    grid, H, d = (21, 30, 52), 2, 128
+    L = 32760
+    q = synth.normal(18, "pk.q", (1, L, H, d)) * 5.0
+    k = synth.normal(18, "pk.k", (1, L, H, d))
+    v = rb(synth.normal(18, "pk.v", (1, L, H, d)))
+    late = np.arange(L) >= L - L // 8
+    growth = np.where(late, 1.0 + 0.6 * (np.arange(L) - (L - L // 8)) / (L // 8), 1.0).astype(np.float32)
+    k = k * growth[None, :, None, None]
+    if qkt == "f16":
+        q, k = (a.astype(np.float16).astype(np.float32) for a in (q, k))
+        QK = torch.float16
+    else:
+        q, k = rb(q), rb(k)
+        QK = BF
+    o = torch.full((1, L, H, d), float("nan"), dtype=BF, device="cuda")
+    wan.wan_attn_rope3d(to_dev(q, QK), to_dev(k, QK), to_dev(v, BF), o, grid, apply_rope=False)
+    wan.wan_sync_status()
+    rows = synth.sample_rows(L, 128, 18)
+    logits = np.einsum("lhd,mhd->hlm", q[0, rows], k[0]) / np.sqrt(d)
+    # the row maxima sit in the late keys for most rows, far above the early keys' maxima
+    assert np.mean(logits.argmax(axis=2) >= L - L // 8) > 0.5
+    assert np.mean(logits.max(axis=2) - logits[:, :, :128].max(axis=2) > 9.0 / np.log2(np.e)) > 0.5
+    assert_bf16_close(to_np(o[0, rows]), O.attention(q[0, rows], k[0], v[0]), f"attn full size peaked {qkt}")
+
+
 # ---------------------------------------------------------------- cross-attention
 
 def test_cross_attn_text_lens(wan):

@@ -142,8 +142,8 @@ int launch_ln_mod_e4m3(const LaunchCtx& c, const float* x, const float* shift, c
 }
 
 // ------------------------------------------------------------------ CFG + Euler
-// x <- x + dt * (vu + s * (vc - vu)), four elements per thread per iteration (16-byte
-// x accesses), grid-stride; a scalar loop takes the n % 4 tail.
+// x <- x + dt * (vu + s * (vc - vu)) on float4 groups (16-byte accesses); a scalar loop
+// takes the n % 4 tail.
 template <typename VT>
 __device__ __forceinline__ void load4(const VT* p, long long i, float* o);
 template <>
@@ -163,22 +163,36 @@ __device__ __forceinline__ float load1(const VT* p, long long i) {
   else return bf2f(p[i]);
 }
 
-template <typename VT>
-__global__ void __launch_bounds__(256) cfg_euler_kernel(float* __restrict__ x, const VT* __restrict__ vc,
+// Each thread takes U float4 groups per pass (g, g + T, ..., g + (U-1) T for T threads in
+// the grid) and issues all their loads before any arithmetic, so every thread keeps 3U
+// 16-byte loads in flight; the grid covers the tensor in one or two passes.
+template <typename VT, int U>
+__global__ void __launch_bounds__(128) cfg_euler_kernel(float* __restrict__ x, const VT* __restrict__ vc,
                                                         const VT* __restrict__ vu, long long n, float s, float dt,
                                                         const float* __restrict__ t_pair) {
   if (t_pair) dt = t_pair[1] - t_pair[0];
   const long long n4 = n >> 2;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < n4; g += stride) {
-    const long long i = g << 2;
-    float a[4], c[4], u[4];
-    load4<float>(x, i, a);
-    load4<VT>(vc, i, c);
-    load4<VT>(vu, i, u);
+  const long long T = (long long)gridDim.x * blockDim.x;
+  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < n4; g += T * U) {
+    float a[U][4], c[U][4], u[U][4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) a[k] = a[k] + dt * (u[k] + s * (c[k] - u[k]));
-    *reinterpret_cast<float4*>(x + i) = make_float4(a[0], a[1], a[2], a[3]);
+    for (int k = 0; k < U; ++k) {
+      const long long gi = g + k * T;
+      if (gi < n4) {
+        load4<float>(x, gi << 2, a[k]);
+        load4<VT>(vc, gi << 2, c[k]);
+        load4<VT>(vu, gi << 2, u[k]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const long long gi = g + k * T;
+      if (gi < n4) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a[k][e] = a[k][e] + dt * (u[k][e] + s * (c[k][e] - u[k][e]));
+        *reinterpret_cast<float4*>(x + (gi << 2)) = make_float4(a[k][0], a[k][1], a[k][2], a[k][3]);
+      }
+    }
   }
   if (blockIdx.x == 0)
     for (long long i = (n4 << 2) + threadIdx.x; i < n; i += blockDim.x) {
@@ -190,17 +204,18 @@ __global__ void __launch_bounds__(256) cfg_euler_kernel(float* __restrict__ x, c
 int launch_cfg_euler(const LaunchCtx& c, float* x, const void* vc, const void* vu, long long n, float s, float dt,
                      const float* t_pair, int v_f32) {
   if (n <= 0) return WAN_OK;
-  long long blocks = ((n >> 2) + 255) / 256;
-  const long long cap = (long long)c.num_sms * 8;
+  constexpr int U = 4, TPB = 128;  // the fastest of a sweep of U x threads per block on this part
+  long long blocks = ((n >> 2) + (long long)TPB * U - 1) / ((long long)TPB * U);
+  const long long cap = (long long)c.num_sms * 32;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   count_launch("cfg_euler", c.stream, true);
   if (v_f32)
-    cfg_euler_kernel<float><<<(unsigned)blocks, 256, 0, c.stream>>>(x, static_cast<const float*>(vc),
-                                                                   static_cast<const float*>(vu), n, s, dt, t_pair);
+    cfg_euler_kernel<float, U><<<(unsigned)blocks, TPB, 0, c.stream>>>(x, static_cast<const float*>(vc),
+                                                                      static_cast<const float*>(vu), n, s, dt, t_pair);
   else
-    cfg_euler_kernel<bf16><<<(unsigned)blocks, 256, 0, c.stream>>>(x, static_cast<const bf16*>(vc),
-                                                                  static_cast<const bf16*>(vu), n, s, dt, t_pair);
+    cfg_euler_kernel<bf16, U><<<(unsigned)blocks, TPB, 0, c.stream>>>(x, static_cast<const bf16*>(vc),
+                                                                     static_cast<const bf16*>(vu), n, s, dt, t_pair);
   count_launch("cfg_euler", c.stream, false);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }

@@ -53,6 +53,10 @@ struct EpiParams {
   // FP8 GEMM: acc[m, n] * a_scale[m] * b_scale[n] before everything above
   const float* a_scale;
   const float* b_scale;
+  // EPI_STORE / EPI_GELU / EPI_GELU_TANH / EPI_QKV: the tile goes out through shared
+  // memory and TMA stores (set by the host when the output allows it) instead of one
+  // row per thread.
+  int tma_store;
 };
 
 // v[i] += bias[n0 + i] with 16-byte vector loads (bias rows are 16-byte aligned and n0
@@ -179,6 +183,27 @@ __device__ __forceinline__ void epi_resid_values(const EpiParams& p, int m, int 
       v[4 * i + 3] *= gg.w;
     }
   }
+}
+
+// The values the store-type epilogues write for row m, columns n0..n0+CNT-1: bias, then
+// GELU, or 3D RoPE on the q / k columns of EPI_QKV.
+template <int CNT>
+__device__ __forceinline__ void epilogue_values(const EpiParams& p, int m, int n0, float* v) {
+  epi_add_bias<CNT>(p, n0, v);
+  if (p.kind == EPI_GELU) {
+#pragma unroll
+    for (int i = 0; i < CNT; ++i) v[i] = gelu_erf(v[i]);
+  } else if (p.kind == EPI_GELU_TANH) {
+#pragma unroll
+    for (int i = 0; i < CNT; ++i) v[i] = gelu_tanh_form(v[i]);
+  } else if (p.kind == EPI_QKV && n0 < p.n_rot) {
+    const int b = m / p.rows_per_batch;
+    epi_rope<CNT>(p.rope, p.head_dim, n0 % p.head_dim, m - b * p.rows_per_batch, v);
+  }
+}
+// Storage type of the store-type epilogues' column n0.
+__device__ __forceinline__ int epilogue_out_type(const EpiParams& p, int n0) {
+  return (p.kind == EPI_QKV && n0 < p.n_f16) ? OUT_F16 : p.out_type;
 }
 
 // Apply the epilogue to values v[0..CNT) of row m, columns n0..n0+CNT-1 (all valid;

@@ -19,7 +19,10 @@
 // stages its 32 x 32 fp32 chunk in shared memory (128-byte swizzle, conflict-free for
 // one-row-per-thread writes) and a TMA reduce-add applies it to x in L2, so the
 // read-modify-write of the fp32 residual stream moves whole lines and leaves no load
-// latency in the epilogue.
+// latency in the epilogue.  The store-type epilogues go out the same way: each warp
+// stages 32 rows x 128 bytes (32 fp32 or 64 16-bit columns) and issues a TMA store.  With
+// one output row per thread, direct stores would send 32 scattered 16-byte pieces per
+// instruction through the SM's memory pipe and hold up the next tile.
 #include <cstdio>
 #include <cstring>
 
@@ -172,6 +175,7 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
     const int ehalf = (warp - 2) >> 2;  // which half of the tile's 32-column chunks
     constexpr int CH = BN / 32 / 2;     // chunks per epilogue warp
     const bool tma_resid = ep.kind == EPI_RESID;
+    const bool tma_out = ep.tma_store != 0;  // tmR then maps the output [M, N]
     float* stage = reinterpret_cast<float*>(epi_stage + (warp - 2) * (32 * 32 * 4));  // [32][32], 1 KB aligned
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -224,6 +228,54 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
               bulk_commit_group();
             }
           }
+        } else if (tma_out) {
+          // 16-bit output: two 32-column chunks fill one 128-byte box row (64 columns;
+          // the host enables this path only when BN >= 128, so a box never spans two
+          // warps' columns); fp32 output: one chunk per box.  Rows past M and columns
+          // past N are clipped by the TMA store.
+          const bool wide = ep.out_type == OUT_F32;
+          const int nbox = wide ? n0 : (n0 & ~63);  // first column of this chunk's box
+          if (row0 < M && nbox < N) {  // warp-uniform
+            const int ot = epilogue_out_type(ep, nbox);
+            uint8_t* buf = reinterpret_cast<uint8_t*>(stage);
+            if (wide || !(c & 1)) {  // the box is about to be refilled
+              if (lane == 0) bulk_wait_group_read<0>();
+              __syncwarp();
+            }
+            const uint32_t row_addr = smem_u32(buf) + lane * 128;
+            if (n0 < N) {
+              float v[32];
+              acc_values(r, n0, v);
+              epilogue_values<32>(ep, row, n0, v);
+              if (wide) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  st_shared_v4(row_addr + ((uint32_t)(j ^ (lane & 7)) << 4),
+                               make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                                          __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3])));
+              } else {
+                const bool h = ot == OUT_F16;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  uint4 u;
+                  const float* w = v + 8 * e;
+                  u.x = h ? pack_half2(w[0], w[1]) : pack_bf16x2(w[0], w[1]);
+                  u.y = h ? pack_half2(w[2], w[3]) : pack_bf16x2(w[2], w[3]);
+                  u.z = h ? pack_half2(w[4], w[5]) : pack_bf16x2(w[4], w[5]);
+                  u.w = h ? pack_half2(w[6], w[7]) : pack_bf16x2(w[6], w[7]);
+                  st_shared_v4(row_addr + ((uint32_t)(((c & 1) * 4 + e) ^ (lane & 7)) << 4), u);
+                }
+              }
+            }
+            if (wide || (c & 1)) {  // the box is complete
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmR, buf, nbox, row0);
+                bulk_commit_group();
+              }
+            }
+          }
         } else if (row < M && n0 < N) {
           float v[32];
           acc_values(r, n0, v);
@@ -236,7 +288,7 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
-    if (tma_resid && lane == 0) bulk_wait_group_all();  // reduces finished before the CTA exits
+    if ((tma_resid || tma_out) && lane == 0) bulk_wait_group_all();  // bulk writes finished before the CTA exits
     __syncwarp();
   }
 
@@ -264,8 +316,37 @@ static int launch_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensor
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
 
+// Tensor map of the epilogue's bulk writes: the fp32 residual x [M, N] (row stride ldr,
+// 32 x 32 boxes) for EPI_RESID; for the store-type epilogues the output [M, N] (32 x 32
+// fp32 boxes, or 64 x 32 16-bit boxes when the tile is at least 128 columns wide), which
+// turns on ep.tma_store.  Other epilogues write directly.
+static int output_map(CUtensorMap* m, EpiParams& ep, int M, int N, int bn) {
+  memset(m, 0, sizeof(*m));
+  ep.tma_store = 0;
+  if (ep.kind == EPI_RESID) {
+    if (ep.ldr % 4 != 0) return WAN_ERR_UNSUPPORTED;
+    return make_tmap_2d(m, ep.resid, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)N, (uint64_t)M,
+                        (uint64_t)ep.ldr * 4, 32, 32);
+  }
+  const bool store_kind = ep.kind == EPI_STORE || ep.kind == EPI_GELU || ep.kind == EPI_GELU_TANH || ep.kind == EPI_QKV;
+  if (!store_kind || !ep.out || (reinterpret_cast<uintptr_t>(ep.out) & 15)) return WAN_OK;
+  if (ep.out_type == OUT_F32) {
+    if (ep.ldo % 4 != 0) return WAN_OK;
+    if (make_tmap_2d(m, ep.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)N, (uint64_t)M, (uint64_t)ep.ldo * 4,
+                     32, 32) != WAN_OK)
+      return WAN_OK;  // direct stores
+  } else {
+    if (bn < 128 || ep.ldo % 8 != 0) return WAN_OK;
+    if (make_tmap_2d(m, ep.out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)N, (uint64_t)M, (uint64_t)ep.ldo * 2,
+                     64, 32) != WAN_OK)
+      return WAN_OK;
+  }
+  ep.tma_store = 1;
+  return WAN_OK;
+}
+
 int gemm_bf16(const LaunchCtx& c, const void* A, long long lda, int a_cols, const void* B, long long ldb, int b_cols,
-              int M, int N, int K, int kb_period, const EpiParams& ep, const char* tag, bool ab_f16) {
+              int M, int N, int K, int kb_period, const EpiParams& ep_in, const char* tag, bool ab_f16) {
   if (M <= 0 || N <= 0 || K <= 0) return WAN_OK;
   int bn = (N % 256 == 0) ? 256 : (N % 128 == 0 ? 128 : 64);
   const CUtensorMapDataType dt = ab_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -275,13 +356,9 @@ int gemm_bf16(const LaunchCtx& c, const void* A, long long lda, int a_cols, cons
   st = make_tmap_2d(&tb, B, dt, 2, (uint64_t)b_cols, (uint64_t)N, (uint64_t)ldb * 2, 64, (uint32_t)bn);
   if (st != WAN_OK) return st;
   CUtensorMap tr;
-  memset(&tr, 0, sizeof(tr));
-  if (ep.kind == EPI_RESID) {  // the fp32 residual x [M, N] (row stride ldr), 32 x 32 boxes
-    if (ep.ldr % 4 != 0) return WAN_ERR_UNSUPPORTED;
-    st = make_tmap_2d(&tr, ep.resid, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)N, (uint64_t)M,
-                      (uint64_t)ep.ldr * 4, 32, 32);
-    if (st != WAN_OK) return st;
-  }
+  EpiParams ep = ep_in;
+  st = output_map(&tr, ep, M, N, bn);
+  if (st != WAN_OK) return st;
   if (ab_f16) {
     switch (bn) {
       case 256: return launch_gemm<256, AB_F16>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
@@ -312,13 +389,8 @@ int gemm_e4m3(const LaunchCtx& c, const uint8_t* A, long long lda, int a_cols, c
   ep.a_scale = sa;
   ep.b_scale = sb;
   CUtensorMap tr;
-  memset(&tr, 0, sizeof(tr));
-  if (ep.kind == EPI_RESID) {
-    if (ep.ldr % 4 != 0) return WAN_ERR_UNSUPPORTED;
-    st = make_tmap_2d(&tr, ep.resid, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)N, (uint64_t)M,
-                      (uint64_t)ep.ldr * 4, 32, 32);
-    if (st != WAN_OK) return st;
-  }
+  st = output_map(&tr, ep, M, N, bn);
+  if (st != WAN_OK) return st;
   switch (bn) {
     case 256: return launch_gemm<256, AB_E4M3>(c, ta, tb, tr, ep, M, N, K, 0, tag);
     case 128: return launch_gemm<128, AB_E4M3>(c, ta, tb, tr, ep, M, N, K, 0, tag);
