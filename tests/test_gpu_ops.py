@@ -134,6 +134,79 @@ def test_adaln_plain_f16_out(wan, B, L, D):
     assert np.max(np.abs(g - ref)) <= 2.0 ** -11 * np.max(np.abs(ref)) + 1e-6, "fp16 LN beyond half an fp16 ulp"
 
 
+@pytest.mark.parametrize("M,N,K", [(1024, 256, 128), (1300, 512, 192), (2 * 1536 + 77, 1536, 320)])
+@pytest.mark.parametrize("epi", ["store_f32", "store_bf16", "gelu", "resid"])
+def test_linear_pair_tiles(wan, M, N, K, epi):
+    # Shapes that run on CTA pairs (N a multiple of 256, M of at least four 256-row tile
+    # pairs): 256-row tiles split over two SMs, a ragged last pair whose second CTA holds
+    # rows past M (or none at all), and every epilogue of the pair kernel.
+    x = rb(synth.normal(19, "lp.x", (M, K)))
+    w = rb(synth.normal(19, "lp.w", (N, K)) * 0.05)
+    b = rb(synth.normal(19, "lp.b", (N,)) * 0.02)
+    y = O.linear(x, w, b)
+    if epi == "resid":
+        rpg = M // 3
+        x0 = synth.normal(19, "lp.x0", (M, N))
+        gate = synth.normal(19, "lp.g", ((M + rpg - 1) // rpg, N))
+        out = to_dev(x0, F32)
+        wan.wan_linear(to_dev(x, BF), to_dev(w, BF), to_dev(b, BF), out, wan.WAN_EPI_RESIDUAL, to_dev(gate, F32), rpg)
+        wan.wan_sync_status()
+        assert_f32_close(to_np(out), x0 + gate[np.arange(M) // rpg] * y, f"pair linear resid {M}x{N}x{K}", tol=1e-4)
+        return
+    dt = F32 if epi == "store_f32" else BF
+    out = torch.full((M, N), float("nan"), dtype=dt, device="cuda")
+    code = wan.WAN_EPI_GELU if epi == "gelu" else wan.WAN_EPI_STORE
+    wan.wan_linear(to_dev(x, BF), to_dev(w, BF), to_dev(b, BF), out, code)
+    wan.wan_sync_status()
+    ref = O.gelu(y) if epi == "gelu" else y
+    if epi == "store_f32":
+        assert_f32_close(to_np(out), ref, f"pair linear {M}x{N}x{K}", tol=1e-4)
+    else:
+        assert_bf16_close(to_np(out), ref, f"pair linear {epi} {M}x{N}x{K}")
+
+
+def test_linear_pair_tiles_f16_and_e4m3(wan):
+    # The fp16 and E4M3 instantiations of the pair kernel (cross-attention projections and
+    # the FP8 variant's GEMMs), fp32 outputs through the residual form.
+    M, N, K = 1500, 768, 256
+    h = lambda a: np.asarray(a, np.float32).astype(np.float16).astype(np.float32)
+    x = h(synth.normal(20, "lq.x", (M, K)))
+    w = h(synth.normal(20, "lq.w", (N, K)) * 0.05)
+    b = rb(synth.normal(20, "lq.b", (N,)) * 0.02)
+    out = torch.zeros((M, N), dtype=F32, device="cuda")
+    wan.wan_linear(to_dev(x, torch.float16), to_dev(w, torch.float16), to_dev(b, BF), out, wan.WAN_EPI_RESIDUAL)
+    wan.wan_sync_status()
+    assert_f32_close(to_np(out), O.linear(x, w, b), "pair linear f16", tol=1e-4)
+    a8, sa = O.quant_rows(x)
+    w8, sw = O.quant_rows(w)
+    dev = lambda z: torch.from_numpy(np.ascontiguousarray(z)).cuda()
+    out = torch.zeros((M, N), dtype=F32, device="cuda")
+    wan.wan_linear_e4m3(dev(a8), dev(sa), dev(w8), dev(sw), to_dev(b, BF), out, wan.WAN_EPI_RESIDUAL)
+    wan.wan_sync_status()
+    assert_f32_close(to_np(out), O.linear_fp8(a8, sa, w8, sw, b), "pair linear e4m3", tol=1e-4)
+
+
+def test_qkv_rope_pair_tiles(wan):
+    # The QKV + RoPE epilogue on pair tiles against the oracle (fp16 q|k, bf16 v).
+    grid, H = (4, 16, 18), 4
+    L, D = 4 * 16 * 18, 512
+    y = rb(synth.normal(21, "qr.y", (1, L, D)))
+    w = rb(synth.normal(21, "qr.w", (3 * D, D)) * 0.05)
+    b = rb(synth.normal(21, "qr.b", (3 * D,)) * 0.02)
+    qkv = torch.full((1, L, 3 * D), float("nan"), dtype=torch.float16, device="cuda")
+    wan.wan_qkv_rope(to_dev(y, BF), to_dev(w, BF), to_dev(b, BF), qkv, H, grid)
+    wan.wan_sync_status()
+    lin = O.linear(y[0], w, b)
+    pos = O.token_positions(grid)
+    q = O.rope3d(O.heads(lin[:, :D], H), pos).reshape(L, D)
+    k = O.rope3d(O.heads(lin[:, D:2 * D], H), pos).reshape(L, D)
+    v = lin[:, 2 * D:]
+    g = qkv[0]
+    assert_bf16_close(to_np(g[:, :D]), q, "qkv rope q")
+    assert_bf16_close(to_np(g[:, D:2 * D]), k, "qkv rope k")
+    assert_bf16_close(to_np(g[:, 2 * D:].contiguous().view(BF)), v, "qkv rope v")
+
+
 @pytest.mark.parametrize("M,N,K", [(47, 96, 128), (130, 512, 256)])
 def test_linear_f32(wan, M, N, K):
     x = synth.normal(5, "lin.x", (M, K))

@@ -31,14 +31,17 @@
 
 namespace wan {
 
-template <int BN>
+// PAIR: the CTA holds half of a 256-row tile pair's A rows and half of its BN B rows
+// (cta_group::2 MMA), so a stage is 16 + 16 KB and six stages fit.
+template <int BN, bool PAIR = false>
 struct GemmCfg {
-  static constexpr int BM = 128;
+  static constexpr int BM = 128;        // rows of A (and of the accumulator) in this CTA
   static constexpr int BK_BYTES = 128;  // one 128-byte swizzle row: 64 bf16 or 128 E4M3
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;
   static constexpr int A_BYTES = BM * BK_BYTES;
-  static constexpr int B_BYTES = BN * BK_BYTES;
+  static constexpr int B_BYTES = B_ROWS * BK_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int STAGES = PAIR ? 6 : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int EPI_WARPS = 8;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
@@ -52,13 +55,17 @@ struct GemmCfg {
 // Operand types of one GEMM instantiation (A and B always share one type).
 enum GemmAB : int { AB_BF16 = 0, AB_F16 = 1, AB_E4M3 = 2 };
 
-template <int BN, int AB>
-__global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
-    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmR, const EpiParams ep, int M, int N, int K,
-                        int kb_period, int* status) {
-  using Cfg = GemmCfg<BN>;
+// The kernel body.  PAIR: one 256 x BN tile per cluster of two CTAs (cta_group::2).  Each
+// CTA loads its own halves of the A and B rows with its own TMA unit (one unit does not
+// keep up with both halves), completing on the leader CTA's (rank 0) stage barrier; the
+// leader issues every MMA and frees each stage in both CTAs; both CTAs' epilogue warps
+// drain their own accumulator rows and free the accumulator on the leader's barrier.
+template <int BN, int AB, bool PAIR>
+__device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmR,
+                                          const EpiParams& ep, int M, int N, int K, int kb_period, int* status) {
+  using Cfg = GemmCfg<BN, PAIR>;
   constexpr bool FP8 = AB == AB_E4M3;
+  constexpr int TILE_M = PAIR ? 256 : 128;  // accumulator rows per tile (over the pair)
   constexpr int BK = FP8 ? 128 : 64;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -72,10 +79,14 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_m = (M + Cfg::BM - 1) / Cfg::BM;
+  const int num_m = (M + TILE_M - 1) / TILE_M;
   const int num_n = (N + BN - 1) / BN;
   const int num_k = (K + BK - 1) / BK;
   const int num_tiles = num_m * num_n;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int tile0 = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int tile_step = PAIR ? (int)cluster_count_x() : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -84,17 +95,23 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], Cfg::EPI_WARPS);  // one arrival per epilogue warp
+      mbar_init(&tempty[a], (PAIR ? 2 : 1) * Cfg::EPI_WARPS);  // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(drain, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, Cfg::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_holder, Cfg::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_holder, Cfg::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before either is signalled
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
@@ -106,38 +123,63 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
     uint32_t phase = 0;
     uint32_t issued = 0, issued_phase = 0;  // bit s: stage s holds a load; its phase
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+    for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
       const int mb = tile / num_n, nb = tile - (tile / num_n) * num_n;
       for (int kb = 0; kb < num_k; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1, status, kDevTimeoutGemm)) { ok = false; break; }
         uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
-        mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
         const int kb_b = kb_period ? (kb % kb_period) : kb;
-        tma_load_2d(sa, &tmA, &full[stage], kb * BK, mb * Cfg::BM);
-        tma_load_2d(sa + Cfg::A_BYTES, &tmB, &full[stage], kb_b * BK, nb * BN);
+        if constexpr (PAIR) {
+          // this CTA's rows mb*256 + rank*128 + [0, 128) of A and nb*BN + rank*BN/2 +
+          // [0, BN/2) of B; the leader's barrier expects both CTAs' bytes (the peer's may
+          // land before the leader's expect_tx: the phase cannot complete before the
+          // leader's arrival)
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * Cfg::STAGE_BYTES);
+          const uint32_t bar = cluster_addr(smem_u32(&full[stage]), 0);
+          const uint32_t dst = smem_u32(sa);
+          tma_load_2d_pair(dst, &tmA, bar, kb * BK, mb * TILE_M + (int)rank * Cfg::BM);
+          tma_load_2d_pair(dst + Cfg::A_BYTES, &tmB, bar, kb_b * BK, nb * BN + (int)rank * Cfg::B_ROWS);
+        } else {
+          mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+          tma_load_2d(sa, &tmA, &full[stage], kb * BK, mb * Cfg::BM);
+          tma_load_2d(sa + Cfg::A_BYTES, &tmB, &full[stage], kb_b * BK, nb * BN);
+        }
         issued |= 1u << stage;
         issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1; }
       }
     }
     if (!ok) {  // error path: let the copies in flight land before the CTA exits
-      for (int s = 0; s < Cfg::STAGES; ++s)
-        if (issued & (1u << s)) {
-          const unsigned long long t0 = globaltimer_ns();
-          while (!mbar_test(&full[s], (issued_phase >> s) & 1u) && globaltimer_ns() - t0 < kWaitLimitNs) {}
-        }
+      if (PAIR && !leader) {
+        // the peer's copies complete on the leader's barriers, which it cannot test:
+        // give them a fixed 50 us (a copy lands in a few)
+        const unsigned long long t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 50000ull) {}
+      } else {
+        for (int s = 0; s < Cfg::STAGES; ++s)
+          if (issued & (1u << s)) {
+            const unsigned long long t0 = globaltimer_ns();
+            while (!mbar_test(&full[s], (issued_phase >> s) & 1u) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+          }
+      }
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1 && lane == 0 && leader) {
     // ---------------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc = FP8 ? make_idesc_e4m3(Cfg::BM, BN)
-                                   : (AB == AB_F16 ? make_idesc_f16(Cfg::BM, BN) : make_idesc_bf16(Cfg::BM, BN));
+    constexpr uint32_t idesc = FP8 ? make_idesc_e4m3(TILE_M, BN)
+                                   : (AB == AB_F16 ? make_idesc_f16(TILE_M, BN) : make_idesc_bf16(TILE_M, BN));
+    // The commits of a pair signal the leader's stage barriers and both CTAs' accumulator
+    // barriers.
+    auto commit = [&](uint64_t* bar) {
+      if constexpr (PAIR) tc_commit_pair(smem_u32(bar));
+      else tc_commit(bar);
+    };
     const uint32_t smem_lo0 = sdesc_sw128_lo(smem_u32(smem));
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+    for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
       if (!mbar_wait(&tempty[acc], acc_phase ^ 1, status, kDevTimeoutGemm)) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
@@ -151,21 +193,27 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
         const uint32_t b_lo = a_lo + (Cfg::A_BYTES >> 4);
 #pragma unroll
         for (int kk = 0; kk < Cfg::BK_BYTES / 32; ++kk) {
-          if constexpr (FP8)
-            tc_mma_ss_f8_lo(d_tmem, a_lo + kk * 2, b_lo + kk * 2, idesc, (kb | kk) != 0 ? 1u : 0u);
-          else
-            tc_mma_ss_lo(d_tmem, a_lo + kk * 2, b_lo + kk * 2, idesc, (kb | kk) != 0 ? 1u : 0u);
+          const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+          if constexpr (PAIR) {
+            if constexpr (FP8) tc_mma_ss_f8_lo_pair(d_tmem, a_lo + kk * 2, b_lo + kk * 2, idesc, accum);
+            else tc_mma_ss_lo_pair(d_tmem, a_lo + kk * 2, b_lo + kk * 2, idesc, accum);
+          } else {
+            if constexpr (FP8) tc_mma_ss_f8_lo(d_tmem, a_lo + kk * 2, b_lo + kk * 2, idesc, accum);
+            else tc_mma_ss_lo(d_tmem, a_lo + kk * 2, b_lo + kk * 2, idesc, accum);
+          }
         }
-        tc_commit(&empty[stage]);
+        commit(&empty[stage]);
+        if constexpr (PAIR) tc_commit_pair(cluster_addr(smem_u32(&empty[stage]), 1));  // the peer's stage
         if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
-      tc_commit(&tfull[acc]);
+      commit(&tfull[acc]);
+      if constexpr (PAIR) tc_commit_pair(cluster_addr(smem_u32(&tfull[acc]), 1));  // the peer's accumulator barrier
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
     if (!ok) {  // error path: wait for the MMAs in flight before TMEM is released
-      tc_commit(drain);
+      commit(drain);
       const unsigned long long t0 = globaltimer_ns();
       while (!mbar_test(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
     }
@@ -179,11 +227,12 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
     float* stage = reinterpret_cast<float*>(epi_stage + (warp - 2) * (32 * 32 * 4));  // [32][32], 1 KB aligned
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    const uint32_t tempty_leader0 = PAIR ? cluster_addr(smem_u32(&tempty[0]), 0) : 0u;
+    for (int tile = tile0; tile < num_tiles; tile += tile_step) {
       const int mb = tile / num_n, nb = tile - (tile / num_n) * num_n;
       if (!mbar_wait_warp(&tfull[acc], acc_phase, status, kDevTimeoutGemm)) break;
       tc_fence_after();
-      const int row0 = mb * Cfg::BM + quad * 32;
+      const int row0 = mb * TILE_M + (int)rank * Cfg::BM + quad * 32;
       const int row = row0 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
       float sa_row = 1.f;
@@ -284,7 +333,10 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if (PAIR && !leader) mbar_arrive_cluster(tempty_leader0 + acc * sizeof(uint64_t));
+        else mbar_arrive(&tempty[acc]);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -294,8 +346,31 @@ __global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // the peer's shared and tensor memory are no longer in use
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    else tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+template <int BN, int AB>
+__global__ void __launch_bounds__(64 + 32 * GemmCfg<BN>::EPI_WARPS, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmR, const EpiParams ep, int M, int N, int K,
+                        int kb_period, int* status) {
+  gemm_body<BN, AB, false>(tmA, tmB, tmR, ep, M, N, K, kb_period, status);
+}
+
+// 256 x 256 tiles over a cluster of two CTAs (cta_group::2): per CTA and K step, 16 KB of
+// A and 16 KB of B, so the L2 -> SM operand stream per FLOP is a third lower than with a
+// 128 x 256 tile per CTA, and six stages are in flight.
+template <int AB>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * GemmCfg<256, true>::EPI_WARPS, 1)
+    gemm_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmR, const EpiParams ep, int M, int N, int K,
+                        int kb_period, int* status) {
+  gemm_body<256, AB, true>(tmA, tmB, tmR, ep, M, N, K, kb_period, status);
 }
 
 template <int BN, int AB>
@@ -315,6 +390,55 @@ static int launch_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensor
   count_launch(tag, c.stream, false);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
+
+template <int AB>
+static int launch_gemm_pair(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr,
+                            const EpiParams& ep, int M, int N, int K, int kb_period, const char* tag) {
+  using Cfg = GemmCfg<256, true>;
+  static std::atomic<unsigned long long> smem_set{0};
+  {
+    const int st = set_smem_limit_once(reinterpret_cast<const void*>(gemm_pair_tc_kernel<AB>), Cfg::SMEM, &smem_set);
+    if (st != WAN_OK) return st;
+  }
+  // Clusters that fit on the GPU at once (a pair needs two free SMs of one GPC, so this can
+  // be below half the SM count); tiles are strided over the resident clusters only.
+  static std::atomic<int> resident[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WAN_ERR_CUDA;
+  int pairs = resident[dev].load(std::memory_order_acquire);
+  if (pairs <= 0) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.gridDim = dim3(c.num_sms, 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(gemm_pair_tc_kernel<AB>), &cfg) !=
+            cudaSuccess ||
+        n <= 0)
+      return WAN_ERR_CUDA;
+    pairs = n < c.num_sms / 2 ? n : c.num_sms / 2;
+    resident[dev].store(pairs, std::memory_order_release);
+  }
+  const int tiles = ((M + 255) / 256) * (N / 256);
+  const int clusters = tiles < pairs ? tiles : pairs;
+  count_launch(tag, c.stream, true);
+  gemm_pair_tc_kernel<AB><<<2 * clusters, Cfg::THREADS, Cfg::SMEM, c.stream>>>(ta, tb, tr, ep, M, N, K, kb_period,
+                                                                               c.dev_status);
+  count_launch(tag, c.stream, false);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+// The CTA-pair GEMM takes the projections whose N is a multiple of 256 and whose M spans
+// at least a few pairs of tiles; the others (the head, small test shapes) stay on one SM
+// per tile.
+static bool use_pair(int M, int N) { return N % 256 == 0 && M >= 4 * 256; }
 
 // Tensor map of the epilogue's bulk writes: the fp32 residual x [M, N] (row stride ldr,
 // 32 x 32 boxes) for EPI_RESID; for the store-type epilogues the output [M, N] (32 x 32
@@ -350,15 +474,19 @@ int gemm_bf16(const LaunchCtx& c, const void* A, long long lda, int a_cols, cons
   if (M <= 0 || N <= 0 || K <= 0) return WAN_OK;
   int bn = (N % 256 == 0) ? 256 : (N % 128 == 0 ? 128 : 64);
   const CUtensorMapDataType dt = ab_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const bool pair = use_pair(M, N);
   CUtensorMap ta, tb;
   int st = make_tmap_2d(&ta, A, dt, 2, (uint64_t)a_cols, (uint64_t)M, (uint64_t)lda * 2, 64, 128);
   if (st != WAN_OK) return st;
-  st = make_tmap_2d(&tb, B, dt, 2, (uint64_t)b_cols, (uint64_t)N, (uint64_t)ldb * 2, 64, (uint32_t)bn);
+  st = make_tmap_2d(&tb, B, dt, 2, (uint64_t)b_cols, (uint64_t)N, (uint64_t)ldb * 2, 64, (uint32_t)(pair ? 128 : bn));
   if (st != WAN_OK) return st;
   CUtensorMap tr;
   EpiParams ep = ep_in;
   st = output_map(&tr, ep, M, N, bn);
   if (st != WAN_OK) return st;
+  if (pair)
+    return ab_f16 ? launch_gemm_pair<AB_F16>(c, ta, tb, tr, ep, M, N, K, kb_period, tag)
+                  : launch_gemm_pair<AB_BF16>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
   if (ab_f16) {
     switch (bn) {
       case 256: return launch_gemm<256, AB_F16>(c, ta, tb, tr, ep, M, N, K, kb_period, tag);
@@ -382,8 +510,9 @@ int gemm_e4m3(const LaunchCtx& c, const uint8_t* A, long long lda, int a_cols, c
   int st = make_tmap_2d(&ta, A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)a_cols, (uint64_t)M, (uint64_t)lda, 128,
                         128);
   if (st != WAN_OK) return st;
+  const bool pair = use_pair(M, N);
   st = make_tmap_2d(&tb, B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)b_cols, (uint64_t)N, (uint64_t)ldb, 128,
-                    (uint32_t)bn);
+                    (uint32_t)(pair ? 128 : bn));
   if (st != WAN_OK) return st;
   EpiParams ep = ep_in;
   ep.a_scale = sa;
@@ -391,6 +520,7 @@ int gemm_e4m3(const LaunchCtx& c, const uint8_t* A, long long lda, int a_cols, c
   CUtensorMap tr;
   st = output_map(&tr, ep, M, N, bn);
   if (st != WAN_OK) return st;
+  if (pair) return launch_gemm_pair<AB_E4M3>(c, ta, tb, tr, ep, M, N, K, 0, tag);
   switch (bn) {
     case 256: return launch_gemm<256, AB_E4M3>(c, ta, tb, tr, ep, M, N, K, 0, tag);
     case 128: return launch_gemm<128, AB_E4M3>(c, ta, tb, tr, ep, M, N, K, 0, tag);

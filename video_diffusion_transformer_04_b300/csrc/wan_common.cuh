@@ -400,6 +400,85 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
 __device__ __forceinline__ float e4m3_inv(float amax) { return amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f; }
 __device__ __forceinline__ float e4m3_deq(float amax) { return __fdiv_rn(amax, 448.f); }
 
+// ------------------------------------------------------------------ CTA pairs (2-SM MMA)
+// A cluster of two CTAs on neighbouring SMs runs one 256-row MMA tile (cta_group::2):
+// each CTA holds half of the A rows and half of the B rows in its own shared memory and
+// receives its half of the accumulator rows in its own tensor memory.  Every tcgen05
+// instruction of such a kernel uses .cta_group::2.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;\n" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;\n" : "=r"(r));
+  return r;
+}
+// The shared::cluster address of the variable at local shared address `addr` in the CTA
+// of the cluster with rank `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// All threads of every CTA of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// One arrival on an mbarrier in another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(bar_cluster_addr) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Arrive once on the mbarrier at shared::cluster address `bar` (this CTA's or the peer's)
+// when every tcgen05 operation issued so far by this thread is done.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+// D (+)= A B^T over the CTA pair: M = 256 rows (128 from each CTA's shared memory at the
+// same offsets), descriptors given by their low words (high word kSdescSw128Hi).
+__device__ __forceinline__ void tc_mma_ss_lo_pair(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .b64 da, db;\n .reg .pred p;\n mov.b64 da, {%1, %5};\n mov.b64 db, {%2, %5};\n"
+      " setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kSdescSw128Hi)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_ss_f8_lo_pair(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .b64 da, db;\n .reg .pred p;\n mov.b64 da, {%1, %5};\n mov.b64 db, {%2, %5};\n"
+      " setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], da, db, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kSdescSw128Hi)
+      : "memory");
+}
+// TMA tile load into the shared memory at shared::cluster address `dst` (this CTA's or
+// the peer's), completing on the mbarrier at shared::cluster address `bar`, which may be
+// in the other CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 // Register budget of a warpgroup after launch (all 128 threads execute it).
 template <int N>
 __device__ __forceinline__ void regs_inc() {
