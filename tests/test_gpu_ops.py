@@ -139,7 +139,8 @@ def test_adaln_plain_f16_out(wan, B, L, D):
 def test_linear_pair_tiles(wan, M, N, K, epi):
     # Shapes that run on CTA pairs (N a multiple of 256, M of at least four 256-row tile
     # pairs): 256-row tiles split over two SMs, a ragged last pair whose second CTA holds
-    # rows past M (or none at all), and every epilogue of the pair kernel.
+    # rows past M (or none at all), and the store and residual epilogues of the pair
+    # kernel (GELU runs on one SM per tile at these shapes).
     x = rb(synth.normal(19, "lp.x", (M, K)))
     w = rb(synth.normal(19, "lp.w", (N, K)) * 0.05)
     b = rb(synth.normal(19, "lp.b", (N,)) * 0.02)

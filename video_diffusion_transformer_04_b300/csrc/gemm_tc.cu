@@ -437,8 +437,12 @@ static int launch_gemm_pair(const LaunchCtx& c, const CUtensorMap& ta, const CUt
 
 // The CTA-pair GEMM takes the projections whose N is a multiple of 256 and whose M spans
 // at least a few pairs of tiles; the others (the head, small test shapes) stay on one SM
-// per tile.
-static bool use_pair(int M, int N) { return N % 256 == 0 && M >= 4 * 256; }
+// per tile.  GELU epilogues stay on one SM too: timed inside the 1.3B step on one B300,
+// the pair takes FFN-down, the output projections and the cross-attention query 3-11 %
+// below the one-SM kernel but the FFN up-projection with its GELU epilogue 2.5 % above it.
+static bool use_pair(int M, int N, const EpiParams& ep) {
+  return N % 256 == 0 && M >= 4 * 256 && ep.kind != EPI_GELU && ep.kind != EPI_GELU_TANH;
+}
 
 // Tensor map of the epilogue's bulk writes: the fp32 residual x [M, N] (row stride ldr,
 // 32 x 32 boxes) for EPI_RESID; for the store-type epilogues the output [M, N] (32 x 32
@@ -474,7 +478,7 @@ int gemm_bf16(const LaunchCtx& c, const void* A, long long lda, int a_cols, cons
   if (M <= 0 || N <= 0 || K <= 0) return WAN_OK;
   int bn = (N % 256 == 0) ? 256 : (N % 128 == 0 ? 128 : 64);
   const CUtensorMapDataType dt = ab_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const bool pair = use_pair(M, N);
+  const bool pair = use_pair(M, N, ep_in);
   CUtensorMap ta, tb;
   int st = make_tmap_2d(&ta, A, dt, 2, (uint64_t)a_cols, (uint64_t)M, (uint64_t)lda * 2, 64, 128);
   if (st != WAN_OK) return st;
@@ -510,7 +514,7 @@ int gemm_e4m3(const LaunchCtx& c, const uint8_t* A, long long lda, int a_cols, c
   int st = make_tmap_2d(&ta, A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)a_cols, (uint64_t)M, (uint64_t)lda, 128,
                         128);
   if (st != WAN_OK) return st;
-  const bool pair = use_pair(M, N);
+  const bool pair = use_pair(M, N, ep_in);
   st = make_tmap_2d(&tb, B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)b_cols, (uint64_t)N, (uint64_t)ldb, 128,
                     (uint32_t)(pair ? 128 : bn));
   if (st != WAN_OK) return st;
