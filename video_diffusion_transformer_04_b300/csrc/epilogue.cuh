@@ -192,7 +192,7 @@ __device__ __forceinline__ void epilogue_values(const EpiParams& p, int m, int n
   epi_add_bias<CNT>(p, n0, v);
   if (p.kind == EPI_GELU) {
 #pragma unroll
-    for (int i = 0; i < CNT; ++i) v[i] = gelu_erf(v[i]);
+    for (int i = 0; i < CNT; i += 2) gelu_erf2(v[i], v[i + 1]);
   } else if (p.kind == EPI_GELU_TANH) {
 #pragma unroll
     for (int i = 0; i < CNT; ++i) v[i] = gelu_tanh_form(v[i]);
@@ -221,7 +221,7 @@ __device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int m, int n0
       break;
     case EPI_GELU:
 #pragma unroll
-      for (int i = 0; i < CNT; ++i) v[i] = gelu_erf(v[i]);
+      for (int i = 0; i < CNT; i += 2) gelu_erf2(v[i], v[i + 1]);
       // fallthrough
     case EPI_STORE:
       epi_store_row<CNT>(p.out, p.out_type, (long long)m * p.ldo + n0, v);

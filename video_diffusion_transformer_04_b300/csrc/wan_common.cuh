@@ -554,4 +554,38 @@ __device__ __forceinline__ float gelu_erf(float x) {
   return 0.5f * x * (1.0f + erf_as7126(x * 0.70710678118654752440f));
 }
 
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;\n" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// gelu_erf on two values: the same operations in the same order (so the same results),
+// with the multiplies and multiply-adds on packed fp32 pairs, which halves the FMA-pipe
+// instructions of the GEMM epilogue.
+__device__ __forceinline__ void gelu_erf2(float& x0, float& x1) {
+  const uint64_t x = f2_pack(x0, x1);
+  const float2 z = f2_unpack(f2_mul(x, f2_pack(0.70710678118654752440f, 0.70710678118654752440f)));
+  const float az0 = fabsf(z.x), az1 = fabsf(z.y);
+  const uint64_t az = f2_pack(az0, az1);
+  const float2 den = f2_unpack(f2_fma(f2_pack(0.3275911f, 0.3275911f), az, f2_pack(1.0f, 1.0f)));
+  float t0, t1;
+  asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(t0) : "f"(den.x));
+  asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(t1) : "f"(den.y));
+  const uint64_t t = f2_pack(t0, t1);
+  uint64_t poly = f2_fma(f2_pack(1.061405429f, 1.061405429f), t, f2_pack(-1.453152027f, -1.453152027f));
+  poly = f2_fma(poly, t, f2_pack(1.421413741f, 1.421413741f));
+  poly = f2_fma(poly, t, f2_pack(-0.284496736f, -0.284496736f));
+  poly = f2_fma(poly, t, f2_pack(0.254829592f, 0.254829592f));
+  const uint64_t npoly = f2_mul(poly, f2_pack(-t0, -t1));  // -(poly * t), exactly
+  const float2 ea = f2_unpack(f2_mul(f2_mul(f2_pack(-az0, -az1), az),
+                                     f2_pack(1.4426950408889634f, 1.4426950408889634f)));
+  const uint64_t e = f2_pack(ex2_approx(ea.x), ex2_approx(ea.y));
+  const float2 y = f2_unpack(f2_fma(npoly, e, f2_pack(1.0f, 1.0f)));
+  const uint64_t erf = f2_pack(copysignf(y.x, z.x), copysignf(y.y, z.y));
+  const float2 g = f2_unpack(f2_mul(f2_mul(f2_pack(0.5f, 0.5f), x), f2_add(f2_pack(1.0f, 1.0f), erf)));
+  x0 = g.x;
+  x1 = g.y;
+}
+
 }  // namespace wan
