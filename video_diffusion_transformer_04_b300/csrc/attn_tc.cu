@@ -48,8 +48,9 @@ struct AttnCfg {
   static constexpr int THREADS = 384;
   // setmaxnreg split of the 384 x 168 registers the CTA launches with:
   // 128 x PRODUCER_REGS + 256 x SOFTMAX_REGS <= 384 x 168.
-  static constexpr int PRODUCER_REGS = 56;
-  static constexpr int SOFTMAX_REGS = 224;
+  // (64 for the producer warpgroup: at 56 the MMA issuer's loop spills.)
+  static constexpr int PRODUCER_REGS = 64;
+  static constexpr int SOFTMAX_REGS = 216;
   static_assert(128 * PRODUCER_REGS + 256 * SOFTMAX_REGS <= 384 * 168, "register split");
   static_assert(HD % 64 == 0, "Q/K/V tiles are whole 64-column (128-byte) boxes");
 };
