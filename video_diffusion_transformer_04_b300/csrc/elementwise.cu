@@ -106,9 +106,83 @@ __global__ void __launch_bounds__(128) ln_mod_kernel(const float* __restrict__ x
   }
 }
 
+// The same pass with one warp per token row (rows up to 2048 wide): the row stays in
+// registers (NV float4 per lane), mean and centred variance reduce by warp shuffles
+// alone, and a 256-thread CTA carries eight rows, so no block barrier sits between a
+// row's loads and its stores.
+template <int NV, typename OutT>
+__global__ void __launch_bounds__(256) ln_mod_warp_kernel(const float* __restrict__ x,
+                                                          const float* __restrict__ shift,
+                                                          const float* __restrict__ scale, long long mod_bstride,
+                                                          OutT* __restrict__ y, int rows, int L, int D, float eps) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int b = row / L;
+  const int nv4 = D >> 2;
+  const float4* xr = reinterpret_cast<const float4*>(x + (long long)row * D);
+  float4 v[NV];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = lane + i * 32;
+    v[i] = c < nv4 ? xr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+    s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float mean = s / (float)D;
+  float q = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    if (lane + i * 32 < nv4) {
+      const float a0 = v[i].x - mean, a1 = v[i].y - mean, a2 = v[i].z - mean, a3 = v[i].w - mean;
+      q += (a0 * a0 + a1 * a1) + (a2 * a2 + a3 * a3);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+  const float rstd = rsqrtf(q / (float)D + eps);
+  const float4* sh = shift ? reinterpret_cast<const float4*>(shift + (long long)b * mod_bstride) : nullptr;
+  const float4* sc = scale ? reinterpret_cast<const float4*>(scale + (long long)b * mod_bstride) : nullptr;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = lane + i * 32;
+    if (c >= nv4) continue;
+    float o0 = (v[i].x - mean) * rstd, o1 = (v[i].y - mean) * rstd;
+    float o2 = (v[i].z - mean) * rstd, o3 = (v[i].w - mean) * rstd;
+    if (sc) {
+      const float4 s4 = sc[c];
+      o0 *= 1.f + s4.x; o1 *= 1.f + s4.y; o2 *= 1.f + s4.z; o3 *= 1.f + s4.w;
+    }
+    if (sh) {
+      const float4 h4 = sh[c];
+      o0 += h4.x; o1 += h4.y; o2 += h4.z; o3 += h4.w;
+    }
+    if constexpr (sizeof(OutT) == 4) {
+      reinterpret_cast<float4*>(y + (long long)row * D)[c] = make_float4(o0, o1, o2, o3);
+    } else if constexpr (std::is_same<OutT, __half>::value) {
+      reinterpret_cast<uint2*>(y + (long long)row * D)[c] = make_uint2(pack_half2(o0, o1), pack_half2(o2, o3));
+    } else {
+      reinterpret_cast<uint2*>(y + (long long)row * D)[c] = make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
+    }
+  }
+}
+
 template <typename OutT>
 static void ln_dispatch(const LaunchCtx& c, const float* x, const float* sh, const float* sc, long long bs, OutT* y,
                         float* sy, int rows, int L, int D, float eps) {
+  if constexpr (sizeof(OutT) != 1) {  // E4M3 output keeps the block kernel (row |max| decision)
+    if (D <= 2048) {
+      const int nw = (D / 4 + 31) / 32;  // float4 per lane
+      const unsigned grid = (unsigned)((rows + 7) / 8);
+      if (nw <= 4) ln_mod_warp_kernel<4, OutT><<<grid, 256, 0, c.stream>>>(x, sh, sc, bs, y, rows, L, D, eps);
+      else if (nw <= 8) ln_mod_warp_kernel<8, OutT><<<grid, 256, 0, c.stream>>>(x, sh, sc, bs, y, rows, L, D, eps);
+      else if (nw <= 12) ln_mod_warp_kernel<12, OutT><<<grid, 256, 0, c.stream>>>(x, sh, sc, bs, y, rows, L, D, eps);
+      else ln_mod_warp_kernel<16, OutT><<<grid, 256, 0, c.stream>>>(x, sh, sc, bs, y, rows, L, D, eps);
+      return;
+    }
+  }
   const int nv = (D / 4 + 127) / 128;
   if (nv <= 1) ln_mod_kernel<1, OutT><<<rows, 128, 0, c.stream>>>(x, sh, sc, bs, y, sy, L, D, eps);
   else if (nv <= 3) ln_mod_kernel<3, OutT><<<rows, 128, 0, c.stream>>>(x, sh, sc, bs, y, sy, L, D, eps);
