@@ -251,9 +251,13 @@ def test_tiny_forward_fp8_variant(wan, bits):
     ctx_o = O.text_projection(inp["text"], w)
     o8 = O.dit_forward(lat, t, ctx_o, None, w, s)
     ex = O.dit_forward(lat, t, ctx_o, None, w, s.replace(fp8=0))
-    _log(what=f"tiny fp8={bits}", kind="fp8_forward", gpu_vs_oracle8=_rel_rms(g, o8), oracle8_vs_exact=_rel_rms(o8, ex),
-         ok=True)
+    e_gpu, e_q, e_exact = _rel_rms(g, o8), _rel_rms(o8, ex), _rel_rms(g, ex)
+    _log(what=f"tiny fp8={bits}", kind="fp8_forward", gpu_vs_oracle8=e_gpu, oracle8_vs_exact=e_q, gpu_vs_exact=e_exact,
+         ok=bool(e_gpu < e_exact))
     assert_bf16_close(g, o8, f"tiny forward fp8={bits}")
+    # the GPU computes the 8-bit variant, not the exact forward: it lies closer to the
+    # 8-bit oracle than to the exact one
+    assert e_gpu < e_exact, f"|gpu - oracle8| {e_gpu:.3e}, |oracle8 - exact| {e_q:.3e}, |gpu - exact| {e_exact:.3e}"
 
 
 @pytest.mark.parametrize("name", ["wan1.3b-block"])
