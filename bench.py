@@ -334,12 +334,16 @@ def run_ours(a, s):
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
+    eclocks = Clocks(gpu_id)  # the e2e pass runs last: its own clock record shows any drift
+    eclocks.start()
+    time.sleep(0.3)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     for _ in range(a.steps):
         step_host()
     f1.record(stream)
     torch.cuda.synchronize(dev)
+    eclk = eclocks.stop()
     ms_e2e = max_over_ranks(f0.elapsed_time(f1), dev)
 
     tokens_per_step = s.batch * s.tokens * max(s.steps, 1)
@@ -396,7 +400,7 @@ def run_ours(a, s):
         "flop_per_step": flop_step,
         "roofline": roof,
         "e2e": {"value": round(aggregate_rate(tokens_per_step, a.steps, world, ms_e2e), 1), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "sm_mhz": eclk.get("sm_mhz")},
         "gpu_launches": launches,
         "clocks": clk,
         "kernels": kernels,
